@@ -1,0 +1,2 @@
+"""Float64 CPU oracle (test infrastructure only; never imported by the product path)."""
+from .sparse_mla_oracle import *  # noqa: F401,F403
