@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark: sparse-MLA paged decode on GB300, microseconds per call.
+
+One step = one decode call (split kernel + merge when nsplit > 1) over one
+batch of synthetic inputs already resident in HBM.  Calls cycle through R
+independent input sets (q, top-k, block table) over one large cache, with
+R * bytes-per-call >= 4 x L2, so every timed call reads rows that are not in
+L2.  Timed on the device with CUDA events around CUDA-graph replays.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-per-config] [--no-cpu-baseline]
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU
+oracle on the host cores (a bounded sample of the same workload, scaled to
+a full call).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/call and achieved HBM GB/s (% roofline) for sparse-MLA decode, B=1..96"
+UNIT = "us/call"
+HEADLINE = "b32_ctx32k"
+ALL_CONFIGS = ["tiny", "bs1_ctx8k", "b32_ctx32k", "b80_ctx128k", "b96_ragged_h64", "b96_ragged_h16"]
+MIN_POOL_PAGES = 65536          # cache pages for rotations of small configs (2.75 GB)
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ----------------------------------------------------------------------------- rank / env helpers
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def reduce_max(value: float, world: int) -> float:
+    """Max of a float over ranks (identity when world == 1)."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def aggregate_us_per_call(max_elapsed_s: float, steps: int, world: int) -> float:
+    """Whole-job microseconds per call: every rank ran `steps` calls in at most max_elapsed_s."""
+    return max_elapsed_s * 1e6 / (steps * world)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_mla_decode_paged_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the split kernel from the committed ncu summary, if it was taken
+    on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "split_kernel_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("traffic_bytes_per_launch", {}).get(workload)
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+    FIELDS = "clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown," \
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown," \
+             "clocks_event_reasons.sw_power_cap"
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+class Bench:
+    def __init__(self, name: str, device, seed_offset: int = 0):
+        import torch
+        from sparse_mla_decode_paged_gb300 import api
+        from sparse_mla_decode_paged_gb300 import workloads as wl
+        self.torch, self.api, self.wl = torch, api, wl
+        self.name = name
+        spec = wl.CONFIGS[name]
+        if seed_offset:
+            import dataclasses
+            spec = dataclasses.replace(spec, seed=spec.seed + 7777 * seed_offset)
+        self.spec = spec
+        self.device = device
+        w0 = wl.make_workload(spec, device=device, pool_pages=MIN_POOL_PAGES)
+        self.cache = w0.kv_cache
+        self.w0 = w0
+        self.bytes_per_call = wl.algorithmic_bytes(w0.topk_idx, w0.seq_lens, w0.block_table, w0.H, w0.num_pages)
+        self.flops_per_call = wl.algorithmic_flops(w0.topk_idx, w0.seq_lens, w0.H)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.l2 = l2
+        self.R = int(min(2048, max(8, math.ceil(4 * l2 / self.bytes_per_call))))
+        self.sets = [w0] + [wl.make_workload(spec, device=device, rotation=r, kv_cache=self.cache)
+                            for r in range(1, self.R)]
+        self.dims = api.dims_of(w0.q, w0.kv_cache, w0.block_table, w0.topk_idx, 0)
+        self.plan = api.plan(self.dims, device.index if hasattr(device, "index") else None)
+        self.nsplit = self.plan.nsplit
+        self.dims.nsplit = self.nsplit
+        self.ws = api.alloc_workspace(self.dims, self.nsplit, device)
+        B, H = w0.B, w0.H
+        self.out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((B, H), dtype=torch.float32, device=device)
+        self.o_part = torch.empty((B, self.nsplit, H, 512), dtype=torch.float32, device=device)
+        self.lse_part = torch.empty((B, self.nsplit, H), dtype=torch.float32, device=device)
+
+    def call(self, i: int):
+        w = self.sets[i % self.R]
+        self.api.sparse_mla_decode(w.q, self.cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                   out=self.out, lse=self.lse, workspace=self.ws, nsplit=self.nsplit)
+
+    def split_only(self, i: int):
+        w = self.sets[i % self.R]
+        d = self.dims
+        lib = self.api._lib()
+        import ctypes as C
+        st = lib.sparse_mla_split(C.byref(d), self.nsplit, self.api._ptr(w.q), self.api._ptr(self.cache),
+                                  self.api._ptr(w.block_table), self.api._ptr(w.topk_idx), self.api._ptr(w.seq_lens),
+                                  C.c_float(w.sm_scale), self.api._ptr(self.o_part), self.api._ptr(self.lse_part),
+                                  self.api._ptr(self.ws), self.api._stream())
+        if st != 0:
+            raise RuntimeError(f"sparse_mla_split failed: {st}")
+
+    def launches_per_call(self) -> int:
+        return 1 + (1 if self.nsplit > 1 else 0)
+
+    def _graph(self, fn, start: int, n: int):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            fn(start)          # warm the path on the capture stream
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                fn(start + i)
+        return g
+
+    def timed(self, fn, steps: int, warmup: int, world: int = 1):
+        """Run warmup calls, then exactly `steps` calls as graph replays; returns max-over-ranks seconds."""
+        torch = self.torch
+        for i in range(warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        G = min(self.R, steps)
+        start = warmup % self.R
+        g_full = self._graph(fn, start, G)
+        reps, tail = divmod(steps, G)
+        g_tail = self._graph(fn, start, tail) if tail else None
+        g_full.replay()                 # one untimed replay: graph upload
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(reps):
+            g_full.replay()
+        if g_tail is not None:
+            g_tail.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        return reduce_max(e0.elapsed_time(e1) / 1e3, world)
+
+    def e2e(self, steps: int, warmup: int):
+        """Per step: H2D of the step's inputs from pinned host memory, the decode call, D2H of out + lse."""
+        torch = self.torch
+        hosts = []
+        for w in self.sets[:min(self.R, 16)]:
+            hosts.append(tuple(t.cpu().pin_memory() for t in (w.q, w.block_table, w.topk_idx, w.seq_lens)))
+        w0 = self.w0
+        dq, dbt, dtk, dsl = (torch.empty_like(t) for t in (w0.q, w0.block_table, w0.topk_idx, w0.seq_lens))
+        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        lse_h = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in hosts[0])
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+
+        def step(i):
+            hq, hbt, htk, hsl = hosts[i % len(hosts)]
+            dq.copy_(hq, non_blocking=True)
+            dbt.copy_(hbt, non_blocking=True)
+            dtk.copy_(htk, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            self.api.sparse_mla_decode(dq, self.cache, dbt, dtk, dsl, w0.sm_scale, out=self.out, lse=self.lse,
+                                       workspace=self.ws, nsplit=self.nsplit)
+            out_h.copy_(self.out, non_blocking=True)
+            lse_h.copy_(self.lse, non_blocking=True)
+
+        for i in range(warmup):
+            step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(steps):
+            step(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / steps, h2d, d2h
+
+
+def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
+    b = Bench(name, device)
+    t = b.timed(b.call, steps, warmup)
+    us = t * 1e6 / steps
+    ts = b.timed(b.split_only, steps, warmup)
+    us_split = ts * 1e6 / steps
+    gbs = b.bytes_per_call / (us * 1e-6) / 1e9
+    res = {"us_per_call": round(us, 3), "split_kernel_us": round(us_split, 3), "nsplit": b.nsplit,
+           "ctas": b.plan.ctas, "algorithmic_bytes": b.bytes_per_call, "gbs": round(gbs, 1),
+           "roofline_frac_call": round(gbs / peak_gbs, 4),
+           "roofline_frac_split_kernel": round(b.bytes_per_call / (us_split * 1e-6) / 1e9 / peak_gbs, 4),
+           "rotations": b.R}
+    del b
+    import torch
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_oracle_sample(name: str, target_s: float = 15.0, max_queries: int = None):
+    """Time the float64 oracle on a bounded sample of the workload on this host; returns
+    (us per full call, queries timed, threads)."""
+    import numpy as np
+    import torch
+    import oracle
+    from sparse_mla_decode_paged_gb300 import workloads as wl
+    import dataclasses
+    spec = wl.CONFIGS[name]
+    # the same recipe for a few queries on the host: per-query oracle work does not depend on the others
+    small = dataclasses.replace(spec, B=min(spec.B, 4), pool_pages=None)
+    w = wl.make_workload(small, device="cpu")
+    q = w.q.view(torch.int16).numpy().view(np.uint16)
+    kv, bt, tk, sl = w.kv_cache.numpy(), w.block_table.numpy(), w.topk_idx.numpy(), w.seq_lens.numpy()
+    done, t0 = 0, time.perf_counter()
+    order = list(range(w.B))
+    while True:
+        b = order[done % w.B]
+        oracle.sparse_mla_decode(q[b:b + 1], kv, bt[b:b + 1], tk[b:b + 1], sl[b:b + 1], w.sm_scale)
+        done += 1
+        el = time.perf_counter() - t0
+        if el >= target_s or (max_queries and done >= max_queries):
+            break
+    per_query = el / done
+    return per_query * spec.B * 1e6, done, w.B
+
+
+def run_cpu_baseline_subprocess(name: str, target_s: float):
+    """Run the oracle timing in a child with BLAS pinned to one thread (so `cores` is exact)."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    code = ("import json,sys; sys.path.insert(0, %r); import bench; "
+            "r = bench.cpu_oracle_sample(%r, %f); print(json.dumps(r))" % (ROOT, name, target_s))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return None
+    us, n, drawn = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{n} single-query oracle runs cycling over {drawn} queries drawn with the {name} recipe "
+                      f"(float64, one thread, ~{target_s:.0f} s), scaled to a full call"}
+
+
+def main_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else torch.cuda.current_device())
+    torch.cuda.set_device(dev)
+    peak, peak_kind = measured_peaks()
+    name = args.workload
+    b = Bench(name, dev, seed_offset=rank)
+    steps = args.steps if args.steps else max(b.R, int(1.0 / 5e-6))
+    visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_index = visible[local] if local < len(visible) else str(local)
+    with ClockSampler(gpu_index) as clk:
+        t = b.timed(b.call, steps, args.warmup, world)
+        ts = b.timed(b.split_only, steps, args.warmup, 1)
+    clocks = clk.summary()
+    us = aggregate_us_per_call(t, steps, world)
+    us_rank = t * 1e6 / steps
+    us_split = ts * 1e6 / steps
+    e2e_us, h2d, d2h = b.e2e(min(steps, 2000), max(3, args.warmup))
+    e2e_us = reduce_max(e2e_us, world) / world
+    achieved = b.bytes_per_call / (us_split * 1e-6) / 1e9
+    line = {
+        "metric": METRIC, "value": round(us, 3), "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(us_rank / 1e3, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp16", "data": "synthetic",
+        "config": {"workload": name, "B": b.w0.B, "H": b.w0.H, "topk": b.w0.topk,
+                   "ctx": b.spec.ctx if b.spec.ctx else "log-uniform 64..524288",
+                   "cache_pages": b.cache.shape[0], "nsplit": b.nsplit, "ctas": b.plan.ctas,
+                   "timing": "CUDA graph replays, events on the launching stream",
+                   "l2": f"inputs larger than L2: {b.R} rotating input sets x {b.bytes_per_call} B "
+                         f">= 4 x L2 ({b.l2} B)",
+                   "parallelism": f"replica per GPU x{world}"},
+        "gbs": round(b.bytes_per_call / (us_rank * 1e-6) / 1e9, 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": recorded_traffic(name),
+                     "kernel": "split", "kernel_us": round(us_split, 3),
+                     "algorithmic_bytes_per_launch": b.bytes_per_call, "peak_source": peak_kind},
+        "e2e": {"value": round(e2e_us, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": steps * b.launches_per_call(),
+        "clocks": clocks,
+    }
+    del b
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_per_config:
+        per = {}
+        for n in ALL_CONFIGS:
+            try:
+                per[n] = measure_config(n, dev, 600 if n in ("tiny", "bs1_ctx8k") else 200, 10, peak)
+            except Exception as e:  # a config that does not fit must not hide the headline line
+                per[n] = {"error": repr(e)[:200]}
+        line["per_config"] = per
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = run_cpu_baseline_subprocess(name, 15.0)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[v] = "1"          # before numpy loads: the oracle runs on exactly one core
+    name = args.workload
+    steps, warmup = args.steps or 5, args.warmup
+    per_step_target = max(0.5, 120.0 / max(1, steps + warmup))
+    for _ in range(warmup):
+        cpu_oracle_sample(name, per_step_target / 4, max_queries=1)
+    vals, cores = [], 1
+    t0 = time.perf_counter()
+    from sparse_mla_decode_paged_gb300 import workloads as wl
+    B = wl.CONFIGS[name].B
+    for _ in range(steps):
+        us, n, _drawn = cpu_oracle_sample(name, per_step_target)
+        vals.append(us)
+    el = time.perf_counter() - t0
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": round(value / 1e3, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": name, "what": "float64 CPU oracle on the host cores; each step times a bounded "
+                                                 "sample of queries and scales to a full call"},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": f"per step >= {per_step_target:.1f} s of oracle work on "
+                                                         f"queries of {name}, scaled to all {B} queries"},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(el, 1)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=0)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=ALL_CONFIGS)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        main_reference(args)
+    else:
+        main_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,186 @@
+/*
+ * sparse_mla.h -- C ABI of the GB300 (sm_103a) sparse-MLA paged decode library.
+ *
+ * One decode query per request b: H query heads attend over the top-k tokens an
+ * indexer selected for b.  The tokens live in a paged FP8 latent cache; each
+ * is gathered through the block table and dequantised, then S = q.k (576
+ * dims: 512 latent + 64 rope), softmax and O = P.v (512 latent dims) run,
+ * split over the top-k list with a log-sum-exp merge of the partial results.
+ *
+ * Sources (page titles and sections of the pages this library follows):
+ *   - "Inside the Decode Performance Investigation: How One Session Cracked the
+ *     Occupancy Ceiling on Blackwell GPUs", Setup (64 query heads,
+ *     index_topk = 512, sparse MLA attention) and Task 1 (split kernel with
+ *     nsplit splits and a combine; attention stalls on scattered FP8
+ *     page-gathers).
+ *   - "The 64-Block Barrier", "The Smoking Gun: Grid = (B, H)" (each block
+ *     walks the top-k tokens: gather, multiply, accumulate) and "The Split-K
+ *     Prescription" (split the top-k set across blocks; merge the partials
+ *     with an online-softmax merge).
+ *   - "The Commit That Rewrote the Bottleneck", "The Levers" (wave-aware split
+ *     count: the grid should be a near multiple of the SM count).
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are caller-owned CUDA device memory, 16-byte aligned,
+ *     dense row-major.  The library never allocates device memory and never
+ *     synchronises the stream (except sparse_mla_read_errors), so every call
+ *     except that one can be captured into a CUDA graph.
+ *   - Work is enqueued on `stream` (NULL = legacy default stream).  A return
+ *     of SMLA_OK means the work was enqueued; a fault inside a kernel shows up
+ *     at the caller's next synchronisation.
+ *   - Host-checkable errors (null pointers, unsupported shapes, small
+ *     workspace) return a status and enqueue nothing.
+ *   - Cache record (656 bytes per token, 64 tokens per page):
+ *       bytes   0..511  latent, FP8 E4M3 (OCP "fn") codes
+ *       bytes 512..527  4 little-endian fp32 scales; latent dim d uses scale[d/128]
+ *       bytes 528..655  64 bf16 rope values
+ *     k[d] = e4m3(code[d]) * scale[d/128] (d < 512), k[512+j] = rope[j];
+ *     v = k[0..511].
+ *   - A top-k entry t of request b is a logical token position.  It is used
+ *     when 0 <= t < seq_lens[b]; its row is block_table[b][t/64]*64 + t%64.
+ *     Other entries (-1 padding, t >= seq_lens[b]) are skipped.  An entry
+ *     below seq_lens[b] whose logical page is >= max_pages_per_seq or whose
+ *     physical page is outside [0, num_pages) is skipped too and sets
+ *     SMLA_DEVERR_PAGE_RANGE in the workspace error word.  Duplicated entries
+ *     count once per occurrence.
+ *   - Outputs: out[b][h][0..511] (bf16) = sum_t softmax_t(s) v_t and
+ *     lse[b][h] (fp32) = ln sum_t exp(s_t), s_t = sm_scale * q[b][h].k_t.  A
+ *     request with no valid entry gets out = 0 and lse = -inf.
+ *   - Numerics: dequantised K/V and the softmax weights are fp16 on chip,
+ *     accumulation is fp32.  |q| and |dequantised latent| must stay below
+ *     65504; larger values saturate and set SMLA_DEVERR_RANGE.
+ */
+#ifndef SPARSE_MLA_H
+#define SPARSE_MLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* smla_stream_t;
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, negative size              */
+  SMLA_ERR_UNSUPPORTED = 2,   /* shape outside what the kernels implement               */
+  SMLA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required             */
+  SMLA_ERR_CUDA = 4           /* a CUDA runtime call or a kernel launch failed          */
+} smla_status;
+
+/* Bits of the device error word kept at the start of the workspace.  They are
+ * OR-ed in by the kernels and stay set until sparse_mla_clear_errors(). */
+#define SMLA_DEVERR_PAGE_RANGE 0x1u  /* a used top-k entry mapped outside the block table or cache */
+#define SMLA_DEVERR_TIMEOUT    0x2u  /* an internal wait gave up; that call's results are invalid  */
+#define SMLA_DEVERR_RANGE      0x4u  /* q or a dequantised latent exceeded the fp16 range          */
+
+typedef struct smla_dims {
+  int32_t batch;              /* B >= 1 decode queries                                   */
+  int32_t num_heads;          /* H in {16, 32, 64, 128}                                  */
+  int32_t topk;               /* top-k entries per query, 1 .. 2048                      */
+  int32_t page_size;          /* tokens per page; must be 64                             */
+  int32_t max_pages_per_seq;  /* row length of block_table, >= 1                         */
+  int32_t d_latent;           /* must be 512                                             */
+  int32_t d_rope;             /* must be 64                                              */
+  int32_t nsplit;             /* partitions of the top-k list; 0 = scheduler's choice    */
+  int64_t num_pages;          /* pages in kv_cache, >= 1                                 */
+} smla_dims;
+
+typedef struct smla_plan {
+  int32_t nsplit;             /* partitions of the top-k list                            */
+  int32_t tokens_per_split;   /* top-k entries per partition (last may be shorter)       */
+  int32_t head_groups;        /* CTAs per (query, partition) along the heads             */
+  int32_t ctas;               /* grid size of the split kernel                           */
+  int32_t ctas_per_sm;        /* CTAs of the split kernel resident per SM                */
+  int32_t sm_count;           /* SMs the plan was made for                               */
+  double waves;               /* ctas / (sm_count * ctas_per_sm)                         */
+  double est_us;              /* cost-model estimate of one call, microseconds           */
+  size_t workspace_bytes;     /* bytes sparse_mla_decode needs with this plan            */
+} smla_plan;
+
+/* Split-count scheduler, host only, no CUDA calls.  Chooses nsplit (unless
+ * dims->nsplit > 0 fixes it) by minimising a wave-quantised cost model over
+ * nsplit in [1, 16]: whole waves of CTAs on sm_count SMs times the per-CTA
+ * time, plus the partial-result traffic and the merge.  Returns
+ * SMLA_ERR_INVALID_ARG for null pointers or sm_count < 1, SMLA_ERR_UNSUPPORTED
+ * for shapes outside smla_dims' stated ranges.  "The Commit That Rewrote the
+ * Bottleneck", "The Levers"; "Inside the Decode Performance Investigation",
+ * Task 1. */
+int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla_plan* plan);
+
+/* As sparse_mla_plan_for, with sm_count read from CUDA device `device`
+ * (cudaDeviceGetAttribute; no allocation, no synchronisation).  Returns
+ * SMLA_ERR_CUDA if the attribute query fails. */
+int sparse_mla_plan(const smla_dims* dims, int32_t device, smla_plan* plan);
+
+/* Workspace bytes sparse_mla_decode needs for `nsplit` partitions: a 256-byte
+ * header (error word) plus, when nsplit > 1, fp32 partials o_part
+ * [B][nsplit][H][512] and lse_part [B][nsplit][H].  Host only.  Returns 0 for
+ * a null or invalid dims. */
+size_t sparse_mla_workspace_size(const smla_dims* dims, int32_t nsplit);
+
+/* Full decode: split kernel (a6) then, when nsplit > 1, the merge (a7).
+ *   q           bf16 [B][H][576]
+ *   kv_cache    uint8 [num_pages][64][656] (record layout above)
+ *   block_table int32 [B][max_pages_per_seq]
+ *   topk_idx    int32 [B][topk]
+ *   seq_lens    int32 [B]
+ *   sm_scale    score scale (1/sqrt(576) for DeepSeek MLA)
+ *   out         bf16 [B][H][512]        (written)
+ *   lse         fp32 [B][H]             (written)
+ *   workspace   >= sparse_mla_workspace_size(dims, plan.nsplit) bytes; its
+ *               first 4 bytes are the device error word.  Concurrent calls
+ *               must not share a workspace.
+ * dims->nsplit = 0 lets the scheduler choose (sparse_mla_plan on the current
+ * device).  Returns SMLA_ERR_WORKSPACE if workspace_bytes is too small. */
+int sparse_mla_decode(const smla_dims* dims, const void* q, const void* kv_cache,
+                      const int32_t* block_table, const int32_t* topk_idx,
+                      const int32_t* seq_lens, float sm_scale, void* out, float* lse,
+                      void* workspace, size_t workspace_bytes, smla_stream_t stream);
+
+/* Split step alone (a1..a6): partition s of query b covers top-k positions
+ * [s*L, min((s+1)*L, topk)) with L = ceil(topk / nsplit).  Writes
+ * o_part [B][nsplit][H][512] = that partition's normalised output (fp32) and
+ * lse_part [B][nsplit][H] = its log-sum-exp (-inf when the partition holds no
+ * valid entry, with o_part = 0).  err_word: device uint32 the kernel ORs
+ * SMLA_DEVERR_* bits into (may be NULL).  "The 64-Block Barrier", "The
+ * Split-K Prescription". */
+int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const void* q, const void* kv_cache,
+                     const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
+                     float sm_scale, float* o_part, float* lse_part, uint32_t* err_word,
+                     smla_stream_t stream);
+
+/* Log-sum-exp merge (a7) of nsplit partials:
+ *   lse[b][h] = ln sum_s exp(lse_part[b][s][h])   (-inf if every partial is -inf)
+ *   out[b][h][d] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h][d]  (bf16; 0 if empty)
+ * nsplit in [1, 64].  "The 64-Block Barrier", "The Split-K Prescription"
+ * (online-softmax merge of the partial results). */
+int sparse_mla_combine(int32_t batch, int32_t num_heads, int32_t nsplit, const float* o_part,
+                       const float* lse_part, void* out, float* lse, smla_stream_t stream);
+
+/* Index -> address step (a1) alone: rows_out[b][i] (int64) = physical row
+ * block_table[b][t/64]*64 + t%64 of top-k entry t = topk_idx[b][i], or -1
+ * when the entry is skipped (rules above).  "Inside the Decode Performance
+ * Investigation", Task 1 (scattered FP8 page-gathers). */
+int sparse_mla_gather_rows(const smla_dims* dims, const int32_t* block_table,
+                           const int32_t* topk_idx, const int32_t* seq_lens, int64_t* rows_out,
+                           smla_stream_t stream);
+
+/* Zero the device error word of a workspace (enqueued on stream). */
+int sparse_mla_clear_errors(void* workspace, smla_stream_t stream);
+
+/* Copy the device error word of a workspace to *flags.  Synchronises `stream`;
+ * not capturable. */
+int sparse_mla_read_errors(const void* workspace, uint32_t* flags, smla_stream_t stream);
+
+/* Static description of a status code. */
+const char* sparse_mla_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPARSE_MLA_H */

@@ -1,0 +1,155 @@
+"""Thin PyTorch binding of the C ABI: argument marshalling only.
+
+Every step of the decode runs in the CUDA library; torch provides device
+memory and the current stream.  Names follow include/sparse_mla.h.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from typing import Optional, Tuple
+
+import torch
+
+from . import _native
+from ._native import SmlaDims, SmlaPlan, check
+
+PAGE_SIZE, D_LATENT, D_ROPE, D_QK = 64, 512, 64, 576
+
+
+def _lib():
+    return _native.load()
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(0)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
+
+
+def make_dims(B: int, H: int, topk: int, max_pages_per_seq: int, num_pages: int, nsplit: int = 0) -> SmlaDims:
+    return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages)
+
+
+def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0) -> SmlaDims:
+    return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit)
+
+
+def plan_for(dims: SmlaDims, sm_count: int) -> SmlaPlan:
+    p = SmlaPlan()
+    check("sparse_mla_plan_for", _lib().sparse_mla_plan_for(C.byref(dims), sm_count, C.byref(p)))
+    return p
+
+
+def plan(dims: SmlaDims, device: Optional[int] = None) -> SmlaPlan:
+    p = SmlaPlan()
+    dev = torch.cuda.current_device() if device is None else device
+    check("sparse_mla_plan", _lib().sparse_mla_plan(C.byref(dims), dev, C.byref(p)))
+    return p
+
+
+def workspace_size(dims: SmlaDims, nsplit: int) -> int:
+    return int(_lib().sparse_mla_workspace_size(C.byref(dims), nsplit))
+
+
+def alloc_workspace(dims: SmlaDims, nsplit: int, device=None) -> torch.Tensor:
+    """Caller-owned workspace (zeroed, so the device error word starts clear)."""
+    n = workspace_size(dims, nsplit)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens):
+    _need(q, "q", torch.bfloat16, 3)
+    _need(kv_cache, "kv_cache", torch.uint8, 3)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if q.shape[2] != D_QK or kv_cache.shape[1] != PAGE_SIZE or kv_cache.shape[2] != 656:
+        raise ValueError("q must be [B,H,576] and kv_cache [pages,64,656]")
+    B = q.shape[0]
+    if block_table.shape[0] != B or topk_idx.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("batch dimensions disagree")
+
+
+def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, topk_idx: torch.Tensor,
+                      seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
+                      lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      nsplit: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0 lets the library's scheduler choose."""
+    _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
+    B, H = q.shape[0], q.shape[1]
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit)
+    if nsplit == 0:
+        nsplit = plan(dims, q.device.index).nsplit
+        dims.nsplit = nsplit
+    if out is None:
+        out = torch.empty((B, H, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(dims, nsplit, q.device)
+    check("sparse_mla_decode", _lib().sparse_mla_decode(
+        C.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens),
+        C.c_float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), C.c_size_t(workspace.numel()),
+        _stream(stream)))
+    return out, lse
+
+
+def sparse_mla_split(q, kv_cache, block_table, topk_idx, seq_lens, sm_scale: float, nsplit: int,
+                     err_word: Optional[torch.Tensor] = None, stream=None):
+    """Partials: o_part fp32 [B,nsplit,H,512], lse_part fp32 [B,nsplit,H]."""
+    _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
+    B, H = q.shape[0], q.shape[1]
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit)
+    o_part = torch.empty((B, nsplit, H, D_LATENT), dtype=torch.float32, device=q.device)
+    lse_part = torch.empty((B, nsplit, H), dtype=torch.float32, device=q.device)
+    check("sparse_mla_split", _lib().sparse_mla_split(
+        C.byref(dims), nsplit, _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens),
+        C.c_float(sm_scale), _ptr(o_part), _ptr(lse_part), _ptr(err_word), _stream(stream)))
+    return o_part, lse_part
+
+
+def sparse_mla_combine(o_part: torch.Tensor, lse_part: torch.Tensor, stream=None):
+    _need(o_part, "o_part", torch.float32, 4)
+    _need(lse_part, "lse_part", torch.float32, 3)
+    B, S, H, D = o_part.shape
+    out = torch.empty((B, H, D), dtype=torch.bfloat16, device=o_part.device)
+    lse = torch.empty((B, H), dtype=torch.float32, device=o_part.device)
+    check("sparse_mla_combine", _lib().sparse_mla_combine(B, H, S, _ptr(o_part), _ptr(lse_part), _ptr(out),
+                                                          _ptr(lse), _stream(stream)))
+    return out, lse
+
+
+def sparse_mla_gather_rows(block_table, topk_idx, seq_lens, num_pages: int, stream=None) -> torch.Tensor:
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(topk_idx, "topk_idx", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    B, K = topk_idx.shape
+    dims = make_dims(B, 64, K, block_table.shape[1], num_pages)
+    rows = torch.empty((B, K), dtype=torch.int64, device=topk_idx.device)
+    check("sparse_mla_gather_rows", _lib().sparse_mla_gather_rows(
+        C.byref(dims), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens), _ptr(rows), _stream(stream)))
+    return rows
+
+
+def clear_errors(workspace: torch.Tensor, stream=None) -> None:
+    check("sparse_mla_clear_errors", _lib().sparse_mla_clear_errors(_ptr(workspace), _stream(stream)))
+
+
+def read_errors(workspace: torch.Tensor, stream=None) -> int:
+    v = C.c_uint32(0)
+    check("sparse_mla_read_errors", _lib().sparse_mla_read_errors(_ptr(workspace), C.byref(v), _stream(stream)))
+    return int(v.value)

@@ -1,0 +1,175 @@
+// C-ABI entry points: argument checks on the host, then kernel launches on
+// the caller's stream.  No allocation, no synchronisation (except
+// sparse_mla_read_errors).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "smla_internal.h"
+
+using namespace smla;
+
+namespace {
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_dims(const smla_dims* d) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1 || d->nsplit < 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
+  if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
+  if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
+  return SMLA_OK;
+}
+
+int check_inputs(const void* q, const void* kv, const int32_t* bt, const int32_t* topk, const int32_t* seq) {
+  if (!q || !kv || !bt || !topk || !seq) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kv, 16) || !aligned(bt, 4) || !aligned(topk, 4) || !aligned(seq, 4))
+    return SMLA_ERR_INVALID_ARG;
+  return SMLA_OK;
+}
+
+int sm_count_of_current_device(int* sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+SplitParams make_params(const smla_dims* d, int nsplit, const void* q, const void* kv, const int32_t* bt,
+                        const int32_t* topk, const int32_t* seq, float sm_scale) {
+  SplitParams p{};
+  p.q = static_cast<const uint16_t*>(q);
+  p.kv = static_cast<const uint8_t*>(kv);
+  p.block_table = bt;
+  p.topk = topk;
+  p.seq_lens = seq;
+  p.sm_scale = sm_scale;
+  p.B = d->batch;
+  p.H = d->num_heads;
+  p.topk_n = d->topk;
+  p.max_pages = d->max_pages_per_seq;
+  p.num_pages = d->num_pages;
+  p.nsplit = nsplit;
+  p.split_len = (d->topk + nsplit - 1) / nsplit;
+  return p;
+}
+
+}  // namespace
+
+extern "C" int sparse_mla_plan(const smla_dims* dims, int32_t device, smla_plan* plan) {
+  if (!dims || !plan || device < 0) return SMLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) return SMLA_ERR_CUDA;
+  return sparse_mla_plan_for(dims, sms, plan);
+}
+
+extern "C" int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const void* q, const void* kv_cache,
+                                const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
+                                float sm_scale, float* o_part, float* lse_part, uint32_t* err_word,
+                                smla_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  st = check_inputs(q, kv_cache, block_table, topk_idx, seq_lens);
+  if (st != SMLA_OK) return st;
+  if (nsplit < 1 || nsplit > kMaxCombineSplit) return SMLA_ERR_INVALID_ARG;
+  if (nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
+  if (!o_part || !lse_part || !aligned(o_part, 16) || !aligned(lse_part, 4)) return SMLA_ERR_INVALID_ARG;
+  if (err_word && !aligned(err_word, 4)) return SMLA_ERR_INVALID_ARG;
+  SplitParams p = make_params(dims, nsplit, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale);
+  p.o_part = o_part;
+  p.lse_part = lse_part;
+  p.err = err_word;
+  p.final_out = false;
+  return launch_split_tc(p, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const void* kv_cache,
+                                 const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
+                                 float sm_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
+                                 smla_stream_t stream) {
+  int st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  st = check_inputs(q, kv_cache, block_table, topk_idx, seq_lens);
+  if (st != SMLA_OK) return st;
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return SMLA_ERR_INVALID_ARG;
+  int nsplit = dims->nsplit;
+  if (nsplit == 0) {
+    int sms = 0;
+    st = sm_count_of_current_device(&sms);
+    if (st != SMLA_OK) return st;
+    smla_plan plan;
+    st = sparse_mla_plan_for(dims, sms, &plan);
+    if (st != SMLA_OK) return st;
+    nsplit = plan.nsplit;
+  }
+  const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, nsplit);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  SplitParams p = make_params(dims, nsplit, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale);
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.final_out = (nsplit == 1);
+  if (nsplit > 1) {
+    const size_t lse_bytes = ((size_t)dims->batch * nsplit * dims->num_heads * sizeof(float) + 255) / 256 * 256;
+    p.lse_part = reinterpret_cast<float*>(ws + kWorkspaceHeader);
+    p.o_part = reinterpret_cast<float*>(ws + kWorkspaceHeader + lse_bytes);
+  }
+  cudaStream_t s = (cudaStream_t)stream;
+  if (launch_split_tc(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (nsplit > 1 &&
+      launch_combine(dims->batch, dims->num_heads, nsplit, p.o_part, p.lse_part, p.out, lse, s) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
+}
+
+extern "C" int sparse_mla_combine(int32_t batch, int32_t num_heads, int32_t nsplit, const float* o_part,
+                                  const float* lse_part, void* out, float* lse, smla_stream_t stream) {
+  if (batch < 1 || num_heads < 1 || nsplit < 1 || nsplit > kMaxCombineSplit) return SMLA_ERR_INVALID_ARG;
+  if (!o_part || !lse_part || !out || !lse) return SMLA_ERR_INVALID_ARG;
+  if (!aligned(o_part, 16) || !aligned(out, 8) || !aligned(lse_part, 4) || !aligned(lse, 4))
+    return SMLA_ERR_INVALID_ARG;
+  return launch_combine(batch, num_heads, nsplit, o_part, lse_part, static_cast<uint16_t*>(out), lse,
+                        (cudaStream_t)stream) == cudaSuccess
+             ? SMLA_OK
+             : SMLA_ERR_CUDA;
+}
+
+extern "C" int sparse_mla_gather_rows(const smla_dims* dims, const int32_t* block_table, const int32_t* topk_idx,
+                                      const int32_t* seq_lens, int64_t* rows_out, smla_stream_t stream) {
+  if (!dims) return SMLA_ERR_INVALID_ARG;
+  if (dims->batch < 1 || dims->topk < 1 || dims->max_pages_per_seq < 1 || dims->num_pages < 1)
+    return SMLA_ERR_INVALID_ARG;
+  if (dims->page_size != kPageSize) return SMLA_ERR_UNSUPPORTED;
+  if (!block_table || !topk_idx || !seq_lens || !rows_out || !aligned(rows_out, 8)) return SMLA_ERR_INVALID_ARG;
+  return launch_gather_rows(block_table, topk_idx, seq_lens, dims->batch, dims->topk, dims->max_pages_per_seq,
+                            dims->num_pages, rows_out, (cudaStream_t)stream) == cudaSuccess
+             ? SMLA_OK
+             : SMLA_ERR_CUDA;
+}
+
+extern "C" int sparse_mla_clear_errors(void* workspace, smla_stream_t stream) {
+  if (!workspace) return SMLA_ERR_INVALID_ARG;
+  return cudaMemsetAsync(workspace, 0, sizeof(uint32_t), (cudaStream_t)stream) == cudaSuccess ? SMLA_OK
+                                                                                            : SMLA_ERR_CUDA;
+}
+
+extern "C" int sparse_mla_read_errors(const void* workspace, uint32_t* flags, smla_stream_t stream) {
+  if (!workspace || !flags) return SMLA_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+      cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+extern "C" const char* sparse_mla_status_string(int status) {
+  switch (status) {
+    case SMLA_OK: return "ok";
+    case SMLA_ERR_INVALID_ARG: return "invalid argument";
+    case SMLA_ERR_UNSUPPORTED: return "unsupported shape";
+    case SMLA_ERR_WORKSPACE: return "workspace missing or too small";
+    case SMLA_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+  }
+}

@@ -1,0 +1,90 @@
+// Log-sum-exp merge of split partials (a7) and the standalone index->address
+// step (a1).
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "smla_device.cuh"
+
+namespace smla {
+namespace {
+
+constexpr int kCombineThreads = 128;   // 4 output dims per thread
+
+// One CTA per (query, head): lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) o_s.
+// "The 64-Block Barrier", "The Split-K Prescription" (online-softmax merge).
+__global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsplit,
+                                                                  const float* __restrict__ o_part,
+                                                                  const float* __restrict__ lse_part,
+                                                                  uint16_t* __restrict__ out,
+                                                                  float* __restrict__ lse) {
+  const int bh = blockIdx.x;
+  const int b = bh / H, h = bh % H;
+  const int tid = threadIdx.x;
+  __shared__ float w_s[kMaxCombineSplit];
+  __shared__ float lse_s;
+  if (tid < 32) {
+    float m = -CUDART_INF_F;
+    for (int s = tid; s < nsplit; s += 32) m = fmaxf(m, __ldg(lse_part + ((size_t)b * nsplit + s) * H + h));
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float z = 0.f;
+    for (int s = tid; s < nsplit; s += 32) {
+      const float l = __ldg(lse_part + ((size_t)b * nsplit + s) * H + h);
+      const float w = (m == -CUDART_INF_F) ? 0.f : expf(l - m);   // exp(-inf) = 0 for empty partials
+      w_s[s] = w;
+      z += w;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    const float inv_z = z > 0.f ? 1.f / z : 0.f;
+    __syncwarp();
+    for (int s = tid; s < nsplit; s += 32) w_s[s] *= inv_z;
+    if (tid == 0) lse_s = z > 0.f ? m + logf(z) : -CUDART_INF_F;
+  }
+  __syncthreads();
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s = 0; s < nsplit; ++s) {
+    const float w = w_s[s];
+    if (w == 0.f) continue;
+    const float4 v = __ldg(reinterpret_cast<const float4*>(o_part + (((size_t)b * nsplit + s) * H + h) * kDLatent) + tid);
+    acc.x = fmaf(w, v.x, acc.x);
+    acc.y = fmaf(w, v.y, acc.y);
+    acc.z = fmaf(w, v.z, acc.z);
+    acc.w = fmaf(w, v.w, acc.w);
+  }
+  uint2 packed;
+  packed.x = f32x2_to_bf16x2(acc.x, acc.y);
+  packed.y = f32x2_to_bf16x2(acc.z, acc.w);
+  reinterpret_cast<uint2*>(out + ((size_t)b * H + h) * kDLatent)[tid] = packed;
+  if (tid == 0) lse[(size_t)b * H + h] = lse_s;
+}
+
+__global__ void gather_rows_kernel(const int32_t* __restrict__ bt, const int32_t* __restrict__ topk,
+                                   const int32_t* __restrict__ seq_lens, int B, int topk_n, int max_pages,
+                                   int64_t num_pages, int64_t* __restrict__ rows) {
+  const int64_t n = (int64_t)B * topk_n;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int b = (int)(i / topk_n);
+    rows[i] = row_of(bt + (size_t)b * max_pages, __ldg(topk + i), __ldg(seq_lens + b), max_pages, num_pages,
+                     nullptr);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part, uint16_t* out,
+                           float* lse, cudaStream_t stream) {
+  combine_kernel<<<B * H, kCombineThreads, 0, stream>>>(H, nsplit, o_part, lse_part, out, lse);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens, int B, int topk_n,
+                               int max_pages, int64_t num_pages, int64_t* rows, cudaStream_t stream) {
+  const int64_t n = (int64_t)B * topk_n;
+  const int threads = 256;
+  const int blocks = (int)((n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096);
+  gather_rows_kernel<<<blocks, threads, 0, stream>>>(bt, topk, seq_lens, B, topk_n, max_pages, num_pages, rows);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

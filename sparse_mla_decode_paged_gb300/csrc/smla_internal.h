@@ -1,0 +1,56 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sparse_mla.h"
+
+namespace smla {
+
+constexpr int kPageSize = 64;
+constexpr int kDLatent = 512;
+constexpr int kDRope = 64;
+constexpr int kDQK = kDLatent + kDRope;   // 576
+constexpr int kRecordBytes = 656;
+constexpr int kMaxTopk = 2048;
+constexpr int kMaxSplit = 16;
+constexpr int kMaxCombineSplit = 64;
+constexpr size_t kWorkspaceHeader = 256;
+
+// Everything the split kernels need for one launch.
+struct SplitParams {
+  const uint16_t* q;          // bf16 [B][H][576]
+  const uint8_t* kv;          // [num_pages][64][656]
+  const int32_t* block_table; // [B][max_pages]
+  const int32_t* topk;        // [B][topk]
+  const int32_t* seq_lens;    // [B]
+  float sm_scale;
+  int B, H, topk_n, max_pages;
+  int64_t num_pages;
+  int nsplit;
+  int split_len;              // top-k positions per partition
+  bool final_out;             // true: write out/lse directly (nsplit == 1); false: partials
+  uint16_t* out;              // bf16 [B][H][512]
+  float* lse;                 // [B][H]
+  float* o_part;              // [B][nsplit][H][512]
+  float* lse_part;            // [B][nsplit][H]
+  uint32_t* err;              // device error word (may be null)
+};
+
+// Kernel launchers (return the launch error).
+cudaError_t launch_split_tc(const SplitParams& p, cudaStream_t stream);
+cudaError_t launch_split_simt(const SplitParams& p, cudaStream_t stream);
+size_t workspace_bytes_for(int B, int H, int nsplit);
+cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part,
+                           uint16_t* out, float* lse, cudaStream_t stream);
+cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens,
+                               int B, int topk_n, int max_pages, int64_t num_pages, int64_t* rows,
+                               cudaStream_t stream);
+
+// Shape limits of the split kernel (checked on the host before any launch).
+bool split_shape_supported(int H, int topk);
+// Resident CTAs per SM of the split kernel for H heads (occupancy of its smem/threads).
+int split_ctas_per_sm(int H);
+
+}  // namespace smla

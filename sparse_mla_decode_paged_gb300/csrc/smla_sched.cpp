@@ -1,0 +1,120 @@
+// Wave-aware split-count scheduler (a8).  Host only; no CUDA calls.
+//
+// The split kernel launches ctas = B * head_groups * nsplit CTAs, of which
+// sm_count * ctas_per_sm run at once.  A grid a little over a whole number of
+// waves pays for a nearly idle extra wave ("The Commit That Rewrote the
+// Bottleneck", "The Levers": 256 CTAs on 188 SMs fill 188 + 68 slots), and
+// more splits shorten each CTA but add partial-result traffic and a merge
+// ("Inside the Decode Performance Investigation", Task 1: split kernel plus
+// combine).  The scheduler evaluates a cost model for every candidate split
+// count and keeps the cheapest (ties: fewer splits).
+#include <math.h>
+#include <string.h>
+
+#include "smla_internal.h"
+
+namespace smla {
+
+// Cost-model constants (microseconds) of the split kernel on GB300: a fixed
+// per-CTA latency (launch, index chain, first loads, tail), a per-token cost
+// for one 64-head group, the per-CTA cost of writing fp32 partials, and the
+// merge kernel.
+struct CostModel {
+  double cta_fixed_us = 2.2;
+  double per_token_us = 0.0095;      // at 64 heads per CTA
+  double partial_write_us = 0.45;    // 64 heads x 512 fp32 per CTA
+  double combine_fixed_us = 1.6;
+  double combine_gbs = 4000.0;       // partial bytes read + out written
+};
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+static bool dims_valid(const smla_dims* d) {
+  if (!d) return false;
+  if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1) return false;
+  if (d->nsplit < 0) return false;
+  return true;
+}
+
+static bool dims_supported(const smla_dims* d) {
+  if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return false;
+  if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return false;
+  return split_shape_supported(d->num_heads, d->topk);
+}
+
+static int split_len_for(int topk, int nsplit) { return (topk + nsplit - 1) / nsplit; }
+
+size_t workspace_bytes_for(int B, int H, int nsplit) {
+  size_t bytes = kWorkspaceHeader;
+  if (nsplit > 1) {
+    bytes += align_up((size_t)B * nsplit * H * sizeof(float), 256);
+    bytes += (size_t)B * nsplit * H * kDLatent * sizeof(float);
+  }
+  return bytes;
+}
+
+static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len,
+                          int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
+  const int head_groups = (H + 63) / 64;
+  const int heads_per_cta = H < 64 ? H : 64;
+  const int ctas = B * head_groups * nsplit;
+  const double slots = (double)sm_count * ctas_per_sm;
+  const double waves = ctas / slots;
+  const int whole_waves = (int)ceil(waves - 1e-9);
+  const int tokens = split_len < topk ? split_len : topk;
+  const double head_frac = heads_per_cta / 64.0;
+  double cta_us = m.cta_fixed_us + m.per_token_us * tokens * (0.5 + 0.5 * head_frac);
+  double t = whole_waves * cta_us;
+  if (nsplit > 1) {
+    t += whole_waves * m.partial_write_us * head_frac;
+    const double bytes = (double)B * H * (nsplit * (kDLatent * 4.0 + 4.0) + kDLatent * 2.0 + 4.0);
+    t += m.combine_fixed_us + bytes / (m.combine_gbs * 1e3);
+  }
+  if (ctas_out) *ctas_out = ctas;
+  if (waves_out) *waves_out = waves;
+  return t;
+}
+
+}  // namespace smla
+
+using namespace smla;
+
+extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla_plan* plan) {
+  if (!dims || !plan || sm_count < 1) return SMLA_ERR_INVALID_ARG;
+  if (!dims_valid(dims)) return SMLA_ERR_INVALID_ARG;
+  if (!dims_supported(dims)) return SMLA_ERR_UNSUPPORTED;
+  const CostModel m;
+  const int B = dims->batch, H = dims->num_heads, K = dims->topk;
+  const int cps = split_ctas_per_sm(H);
+  int best_n = -1, best_len = 0, best_ctas = 0;
+  double best_t = 0, best_w = 0;
+  int lo = 1, hi = kMaxSplit;
+  if (dims->nsplit > 0) lo = hi = dims->nsplit;
+  for (int n = lo; n <= hi; ++n) {
+    const int len = split_len_for(K, n);
+    // an automatic choice never leaves a partition empty; a fixed one is kept as given
+    if (dims->nsplit == 0 && (K + len - 1) / len != n) continue;
+    int ctas;
+    double w;
+    const double t = estimate_us(m, B, H, K, n, len, sm_count, cps, &ctas, &w);
+    if (best_n < 0 || t < best_t - 1e-9) {
+      best_n = n; best_len = len; best_t = t; best_ctas = ctas; best_w = w;
+    }
+  }
+  memset(plan, 0, sizeof(*plan));
+  plan->nsplit = best_n;
+  plan->tokens_per_split = best_len;
+  plan->head_groups = (H + 63) / 64;
+  plan->ctas = best_ctas;
+  plan->ctas_per_sm = cps;
+  plan->sm_count = sm_count;
+  plan->waves = best_w;
+  plan->est_us = best_t;
+  plan->workspace_bytes = workspace_bytes_for(B, H, best_n);
+  return SMLA_OK;
+}
+
+extern "C" size_t sparse_mla_workspace_size(const smla_dims* dims, int32_t nsplit) {
+  if (!dims_valid(dims) || nsplit < 1) return 0;
+  return workspace_bytes_for(dims->batch, dims->num_heads, nsplit);
+}

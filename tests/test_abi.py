@@ -1,0 +1,121 @@
+"""The C-ABI library loads, exports every declared entry point, and rejects bad
+arguments on the host (no GPU needed: nothing here launches a kernel)."""
+import ctypes as C
+import glob
+import math
+import os
+import re
+
+import pytest
+
+import oracle
+from sparse_mla_decode_paged_gb300 import _native
+from sparse_mla_decode_paged_gb300.api import make_dims
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names |= set(re.findall(r"\b(sparse_mla_\w+)\s*\(", txt))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code, name in _native.STATUS.items():
+        assert lib.sparse_mla_status_string(code)
+    assert lib.sparse_mla_status_string(99) == b"unknown status"
+
+
+FAKE = C.c_void_p(1 << 20)   # aligned non-null stand-in; never dereferenced by these calls
+
+
+def _decode(lib, dims, ws=FAKE, ws_bytes=1 << 30, q=FAKE):
+    return lib.sparse_mla_decode(C.byref(dims), q, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,
+                                 ws, C.c_size_t(ws_bytes), None)
+
+
+def test_host_side_rejections(lib):
+    d = make_dims(4, 64, 512, 16, 100, nsplit=4)
+    assert _decode(lib, d, q=C.c_void_p(0)) == 1                      # null q
+    assert _decode(lib, d, q=C.c_void_p((1 << 20) + 8)) == 1          # misaligned q
+    bad = make_dims(4, 64, 512, 16, 100, nsplit=4); bad.page_size = 32
+    assert _decode(lib, bad) == 2
+    bad = make_dims(4, 48, 512, 16, 100, nsplit=4)
+    assert _decode(lib, bad) == 2                                     # unsupported head count
+    bad = make_dims(4, 64, 4096, 16, 100, nsplit=4)
+    assert _decode(lib, bad) == 2                                     # top-k too long
+    bad = make_dims(0, 64, 512, 16, 100, nsplit=4)
+    assert _decode(lib, bad) == 1
+    need = lib.sparse_mla_workspace_size(C.byref(d), 4)
+    assert need == 256 + 4 * 4 * 64 * 4 + 4 * 4 * 64 * 512 * 4
+    assert _decode(lib, d, ws_bytes=need - 1) == 3                    # workspace too small
+    assert _decode(lib, d, ws=C.c_void_p(0)) == 3
+    assert lib.sparse_mla_combine(4, 64, 0, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert lib.sparse_mla_combine(4, 64, 65, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert lib.sparse_mla_split(C.byref(d), 0, FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(1.0), FAKE, FAKE,
+                                None, None) == 1
+    assert lib.sparse_mla_gather_rows(None, FAKE, FAKE, FAKE, FAKE, None) == 1
+    assert lib.sparse_mla_read_errors(None, None, None) == 1
+    assert lib.sparse_mla_workspace_size(None, 2) == 0
+
+
+def _plan(lib, B, H, K, sms, nsplit=0):
+    p = _native.SmlaPlan()
+    st = lib.sparse_mla_plan_for(C.byref(make_dims(B, H, K, 8192, 1 << 20, nsplit)), sms, C.byref(p))
+    assert st == 0
+    return p
+
+
+def test_plan_fields_consistent(lib):
+    for B in (1, 7, 32, 64, 80, 96):
+        for H in (16, 64, 128):
+            p = _plan(lib, B, H, 512, 152)
+            assert 1 <= p.nsplit <= 16
+            assert p.tokens_per_split == math.ceil(512 / p.nsplit)
+            assert math.ceil(512 / p.tokens_per_split) == p.nsplit          # no empty partition
+            assert p.head_groups == max(1, H // 64)
+            assert p.ctas == B * p.head_groups * p.nsplit
+            assert abs(p.waves - p.ctas / (152 * p.ctas_per_sm)) < 1e-12
+            ws = 256 if p.nsplit == 1 else 256 + math.ceil(B * p.nsplit * H * 4 / 256) * 256 + B * p.nsplit * H * 2048
+            assert p.workspace_bytes == ws
+
+
+def test_plan_is_argmin_of_its_cost_model(lib):
+    """The automatic choice is the cheapest fixed choice (brute force over 1..16)."""
+    for B in range(1, 97, 5):
+        for sms in (148, 152, 188):
+            auto = _plan(lib, B, 64, 512, sms)
+            costs = {}
+            for n in range(1, 17):
+                if math.ceil(512 / math.ceil(512 / n)) != n:
+                    continue
+                costs[n] = _plan(lib, B, 64, 512, sms, nsplit=n).est_us
+            best = min(costs.values())
+            assert auto.est_us == pytest.approx(best)
+            assert auto.nsplit == min(n for n, c in costs.items() if c <= best + 1e-9)
+
+
+def test_plan_fixed_split_kept(lib):
+    p = _plan(lib, 4, 64, 10, 152, nsplit=16)
+    assert p.nsplit == 16 and p.tokens_per_split == 1
+
+
+def test_wave_count_matches_pages_arithmetic(lib):
+    """With the pages' grid (B * 2 head groups * nsplit) the waves are the pages' numbers."""
+    for B in (32, 96):
+        ctas = oracle.pages_grid(B)
+        assert round(ctas / 188, 2) == {32: 1.36, 96: 2.04}[B]
+    p = _plan(lib, 64, 128, 512, 188, nsplit=2)     # 2 head groups of 64, as in the pages' B=64 case
+    assert p.ctas == 256 and round(p.waves, 2) == round(256 / 188, 2)
+    assert round(1 - oracle.wave_efficiency(p.ctas, 188), 2) == 0.32

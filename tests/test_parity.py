@@ -1,0 +1,136 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_mla_decode_paged_gb300 import api
+from sparse_mla_decode_paged_gb300 import workloads as wl
+from parity_util import compare, oracle_on, oracle_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run(w, nsplit=0):
+    out, lse = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                     nsplit=nsplit)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+def _custom(B, H, topk, ctx, seed, **kw):
+    return wl.make_custom(B=B, H=H, topk=topk, ctx_lens=ctx, seed=seed, device=DEV, **kw)
+
+
+def test_tiny_config():
+    w = wl.make_workload(wl.CONFIGS["tiny"], device=DEV)
+    out, lse = _run(w)
+    compare(out, lse, *oracle_on(w))
+
+
+@pytest.mark.parametrize("H", [16, 32, 64, 128])
+def test_ragged_small_all_head_counts(H):
+    # several tiles per partition, a ragged tail, padding (ctx < topk), a one-token context
+    w = _custom(B=5, H=H, topk=300, ctx=[1000, 250, 64, 1, 5000], seed=20 + H, outlier_channels=5)
+    out, lse = _run(w)
+    compare(out, lse, *oracle_on(w))
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 3, 4, 7, 8, 13, 16])
+def test_every_split_count(nsplit):
+    w = _custom(B=3, H=64, topk=512, ctx=[4096, 700, 300], seed=31)
+    out, lse = _run(w, nsplit=nsplit)
+    compare(out, lse, *oracle_on(w))
+
+
+def test_split_and_combine_entry_points():
+    w = _custom(B=2, H=64, topk=200, ctx=[900, 150], seed=32)
+    o_part, lse_part = api.sparse_mla_split(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale, 3)
+    torch.cuda.synchronize()
+    q, kv, bt, tk, sl = wl.host_subset(w, range(w.B))
+    o_ref, l_ref = oracle.split_partials(q.view(torch.int16).numpy().view(np.uint16), kv.numpy(), bt.numpy(),
+                                         tk.numpy(), sl.numpy(), w.sm_scale, 3)
+    for s in range(3):
+        compare(o_part[:, s].clone(), lse_part[:, s].clone(), o_ref[:, s], l_ref[:, s])
+    out, lse = api.sparse_mla_combine(o_part, lse_part)
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle.combine(o_ref, l_ref))
+
+
+def test_edge_cases_padding_empty_duplicates():
+    w = _custom(B=6, H=64, topk=64, ctx=[300, 300, 300, 300, 0, 70], seed=33)
+    w.topk_idx[0] = -1                                   # all padding
+    w.topk_idx[1, :] = -1
+    w.topk_idx[1, 17] = 123                              # one valid token
+    w.topk_idx[2, :8] = torch.tensor([5, 5, 5, 9, 9, 299, 300, 10_000], dtype=torch.int32, device=DEV)  # dups, bounds
+    w.topk_idx[3] = w.topk_idx[3].flip(0)
+    out, lse = _run(w)
+    ref_out, ref_lse = oracle_on(w)
+    compare(out, lse, ref_out, ref_lse)
+    assert torch.all(out[0] == 0) and torch.all(torch.isneginf(lse[0]))
+    assert torch.all(torch.isneginf(lse[4]))
+
+
+@pytest.mark.parametrize("topk,ctx", [(1, [5, 1]), (2048, [3000, 2048]), (17, [17, 400])])
+def test_topk_extremes(topk, ctx):
+    w = _custom(B=2, H=64, topk=topk, ctx=ctx, seed=34 + topk)
+    out, lse = _run(w)
+    compare(out, lse, *oracle_on(w))
+
+
+def test_bad_pages_are_skipped_and_flagged():
+    w = _custom(B=2, H=64, topk=64, ctx=[500, 500], seed=35)
+    ref_w = _custom(B=2, H=64, topk=64, ctx=[500, 500], seed=35)
+    w.block_table[0, 2] = w.num_pages + 7               # physical page outside the cache
+    w.block_table[1, 0] = -3
+    dims = api.dims_of(w.q, w.kv_cache, w.block_table, w.topk_idx, 2)
+    ws = api.alloc_workspace(dims, 2)
+    out, lse = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                     workspace=ws, nsplit=2)
+    flags = api.read_errors(ws)
+    assert flags & 0x1
+    compare(out, lse, *oracle_on(w))                     # the oracle skips the same entries
+    api.clear_errors(ws)
+    out2, lse2 = api.sparse_mla_decode(ref_w.q, ref_w.kv_cache, ref_w.block_table, ref_w.topk_idx,
+                                       ref_w.seq_lens, ref_w.sm_scale, workspace=ws, nsplit=2)
+    assert api.read_errors(ws) == 0
+
+
+def test_gather_rows_bit_exact_small():
+    w = _custom(B=4, H=64, topk=100, ctx=[5000, 90, 1, 640], seed=36)
+    w.topk_idx[0, 3] = 5000
+    w.topk_idx[0, 4] = -1
+    rows = api.sparse_mla_gather_rows(w.block_table, w.topk_idx, w.seq_lens, w.num_pages)
+    torch.cuda.synchronize()
+    assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))
+
+
+def _sample(B, n, seed):
+    rng = np.random.default_rng(seed)
+    return sorted(rng.choice(B, size=min(n, B), replace=False).tolist())
+
+
+@pytest.mark.parametrize("name", ["bs1_ctx8k", "b32_ctx32k", "b80_ctx128k", "b96_ragged_h64", "b96_ragged_h16"])
+def test_full_size_configs_sampled(name):
+    """The full configurations with the scheduler's launch choice (the one the benchmark times):
+    every gathered row index is bit-exact for all queries; out and lse are checked against the oracle on
+    sampled queries (the oracle copies only the pages those queries touch)."""
+    w = wl.make_workload(wl.CONFIGS[name], device=DEV)
+    try:
+        out, lse = _run(w)
+        rows = api.sparse_mla_gather_rows(w.block_table, w.topk_idx, w.seq_lens, w.num_pages)
+        torch.cuda.synchronize()
+        assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))
+        idx = _sample(w.B, 6, seed=len(name))
+        if name.startswith("b96"):
+            lens = w.seq_lens.cpu().numpy()
+            idx = sorted(set(idx) | {int(np.argmin(lens)), int(np.argmax(lens))})   # shortest and longest context
+        ref_out, ref_lse = oracle_on(w, idx)
+        compare(out[idx], lse[idx], ref_out, ref_lse)
+        assert torch.isfinite(lse[w.seq_lens > 0]).all()
+    finally:
+        del w
+        torch.cuda.empty_cache()
