@@ -156,7 +156,7 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- our arm
 
 class Bench:
-    def __init__(self, name: str, device, seed_offset: int = 0):
+    def __init__(self, name: str, device, seed_offset: int = 0, nsplit: int = 0):
         import torch
         from sparse_mla_decode_paged_gb300 import api
         from sparse_mla_decode_paged_gb300 import workloads as wl
@@ -179,6 +179,7 @@ class Bench:
         self.sets = [w0] + [wl.make_workload(spec, device=device, rotation=r, kv_cache=self.cache)
                             for r in range(1, self.R)]
         self.dims = api.dims_of(w0.q, w0.kv_cache, w0.block_table, w0.topk_idx, 0)
+        self.dims.nsplit = nsplit
         self.plan = api.plan(self.dims, device.index if hasattr(device, "index") else None)
         self.nsplit = self.plan.nsplit
         self.dims.nsplit = self.nsplit
