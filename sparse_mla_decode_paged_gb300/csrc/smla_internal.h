@@ -52,5 +52,7 @@ cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int
 bool split_shape_supported(int H, int topk);
 // Resident CTAs per SM of the split kernel for H heads (occupancy of its smem/threads).
 int split_ctas_per_sm(int H);
+// Heads handled by one CTA of the split kernel (H is split into ceil(H / this) groups).
+int split_heads_per_cta();
 
 }  // namespace smla

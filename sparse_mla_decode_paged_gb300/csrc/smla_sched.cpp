@@ -21,8 +21,8 @@ namespace smla {
 // merge kernel.
 struct CostModel {
   double cta_fixed_us = 2.2;
-  double per_token_us = 0.0095;      // at 64 heads per CTA
-  double partial_write_us = 0.45;    // 64 heads x 512 fp32 per CTA
+  double per_token_us = 0.0095;      // per top-k entry for one CTA's head group
+  double partial_write_us = 0.25;    // one head group x 512 fp32 per CTA
   double combine_fixed_us = 1.6;
   double combine_gbs = 4000.0;       // partial bytes read + out written
 };
@@ -55,14 +55,15 @@ size_t workspace_bytes_for(int B, int H, int nsplit) {
 
 static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len,
                           int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
-  const int head_groups = (H + 63) / 64;
-  const int heads_per_cta = H < 64 ? H : 64;
+  const int hpc = split_heads_per_cta();
+  const int head_groups = (H + hpc - 1) / hpc;
+  const int heads_per_cta = H < hpc ? H : hpc;
   const int ctas = B * head_groups * nsplit;
   const double slots = (double)sm_count * ctas_per_sm;
   const double waves = ctas / slots;
   const int whole_waves = (int)ceil(waves - 1e-9);
   const int tokens = split_len < topk ? split_len : topk;
-  const double head_frac = heads_per_cta / 64.0;
+  const double head_frac = (double)heads_per_cta / hpc;
   double cta_us = m.cta_fixed_us + m.per_token_us * tokens * (0.5 + 0.5 * head_frac);
   double t = whole_waves * cta_us;
   if (nsplit > 1) {
@@ -104,7 +105,7 @@ extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla
   memset(plan, 0, sizeof(*plan));
   plan->nsplit = best_n;
   plan->tokens_per_split = best_len;
-  plan->head_groups = (H + 63) / 64;
+  plan->head_groups = (H + split_heads_per_cta() - 1) / split_heads_per_cta();
   plan->ctas = best_ctas;
   plan->ctas_per_sm = cps;
   plan->sm_count = sm_count;

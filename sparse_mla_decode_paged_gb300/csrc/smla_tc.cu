@@ -1,28 +1,38 @@
 // Tensor-core split kernel (sm_103a): tcgen05 MMAs with TMEM accumulators.
 //
-// One CTA per (partition s of the top-k list, group of 64 heads, query b).
+// One CTA per (partition s of the top-k list, group of 32 heads, query b).
 // The partition is walked in tiles of 128 top-k entries:
 //
-//   gather warps (8)   index -> row through the block table (a1), 16-byte
+//   gather warps (8)   index -> row through the block table (a1); 16-byte
 //                      streaming loads of each 656-byte record into
-//                      registers, dequantisation (E4M3 * fp32 block scale,
-//                      bf16 rope) to fp16 (a2), stored 128B-swizzled into the
-//                      K tile in 9 chunks of 64 dims; the next tile's loads
-//                      are issued as soon as a tile is stored.
-//   MMA warp (1 lane)  S^T[128 tok x 64 heads] = K[tok x 576] . Q^T   (a3)
-//                      36 MMAs M=128 N=64 K=16, accumulator in TMEM; then
-//                      O^T[512 x 64] += V^T[512 x tok] . P^T            (a5)
-//                      4 blocks of 128 dims x 8 MMAs; V^T is the latent
-//                      part of the same K tile read MN-major.
-//   softmax warps (4)  one TMEM lane (token) per thread: per-head running
-//                      max across the tile (warp reduce-scatter + shared
-//                      memory), P = exp2(s - m) in fp16 written over the rope
-//                      chunk (a4), lazy rescale of O when a head's max grows
-//                      by more than 2^8, and the epilogue (a6): O / l and lse.
+//                      registers; the E4M3 latent codes are converted to fp16
+//                      exactly (every E4M3 value is an fp16 value) and the bf16
+//                      rope to fp16 (a2), stored 128B-swizzled into the K tile
+//                      (9 chunks of 64 dims); the four fp32 scales of each
+//                      token go to shared memory.  The next tile's loads are
+//                      issued as soon as a tile is stored.
+//   MMA warp (1 lane)  QK per scale block: S_b^T[128 tok x 32 heads] =
+//                      K_b . Q_b^T for the four 128-dim latent blocks and the
+//                      rope (a3), M=128 N=32, five fp32 TMEM accumulators;
+//                      then O_j^T[128 dims x 32 heads] += V_j^T . P_j^T for the
+//                      four dim blocks (a5), V_j^T being the same codes read
+//                      MN-major and P_j = P scaled by the tokens' block-j scale.
+//   softmax warps (4)  one TMEM lane (token) per thread: exact score
+//                      s = sum_b scale_b S_b + S_rope in fp32; per-head
+//                      running max over the tile (warp reduce-scatter + shared
+//                      memory), P = exp2(s - m) (a4), the four scaled P_j in
+//                      fp16, lazy rescale of O when a head's max grows by more
+//                      than 2^8, and the epilogue (a6): O / l and lse.
 //
-// Shared memory: Q 72 KB (64 heads x 576 fp16) + K tile 144 KB (128 x 576
-// fp16) + barriers: one CTA per SM, 13 warps.  TMEM: O^T in columns 0..255,
-// S^T in 256..319 (512 allocated).
+// Keeping the latent codes unscaled makes every product in QK exact, so the
+// scores carry fp32 accumulation error only; the per-block scales enter in
+// fp32 in the softmax and, for PV, through P_j.  P_j carries a per-CTA power
+// of two F_j (fixed at the first tile with data) so that it sits in the fp16
+// normal range; the epilogue divides it out.
+//
+// Shared memory: Q 36 KB (32 heads x 576 fp16) + K tile 144 KB (128 x 576
+// fp16) + P 32 KB (4 x 32 heads x 128 tokens fp16) + barriers: one CTA per
+// SM, 13 warps.  TMEM: O^T in columns 0..127, S in 128..287 (512 allocated).
 // Sources: "The 64-Block Barrier" ("The Smoking Gun", "The Split-K
 // Prescription"); "Inside the Decode Performance Investigation" (Task 1).
 #include <cuda_runtime.h>
@@ -34,24 +44,27 @@
 namespace smla {
 namespace {
 
-constexpr int kTile = 128;                 // top-k entries per tile (MMA M for S^T)
-constexpr int kHeads = 64;                 // heads per CTA (MMA N), padded with zero rows when H < 64
+constexpr int kTile = 128;                 // top-k entries per tile (MMA M)
+constexpr int kHeads = 32;                 // heads per CTA (MMA N), zero rows past the valid heads
 constexpr int kChunks = 9;                 // 576 dims / 64
-constexpr int kQChunkBytes = kHeads * 128;
-constexpr int kKChunkBytes = kTile * 128;
-constexpr int kQBytes = kChunks * kQChunkBytes;     // 73728
-constexpr int kKBytes = kChunks * kKChunkBytes;     // 147456
+constexpr int kQChunkBytes = kHeads * 128;               // 4 KB
+constexpr int kKChunkBytes = kTile * 128;                // 16 KB
+constexpr int kPChunkBytes = kHeads * 128;               // 32 heads x 64 tokens
+constexpr int kPBytes = 2 * kPChunkBytes;                // one P_j: 2 chunks of 64 tokens
+constexpr int kQBytes = kChunks * kQChunkBytes;          // 36864
+constexpr int kKBytes = kChunks * kKChunkBytes;          // 147456
+constexpr int kPAllBytes = 4 * kPBytes;                  // 32768
 constexpr int kThreads = 416;
 constexpr int kSoftmaxThreads = 128;       // warps 0..3 (TMEM lane quadrants 0..3)
 constexpr int kGatherThreads = 256;        // warps 4..11
 constexpr int kMmaWarp = 12;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256 in fp16
+constexpr uint32_t kSCol = 128;            // S_b at kSCol + 32 b, b = 0..4 (4 = rope)
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 constexpr float kFp16Max = 65504.0f;
 
 constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kHeads, 0, 0);
-constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
+constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 0);
 
 struct Misc {
   uint64_t q_ready, meta_ready, s_full, p_ready, pv_done, teardown;
@@ -62,25 +75,27 @@ struct Misc {
   int need_rescale;
   int stop;
   int range_err;
+  int f_set;
+  int scmax[4];                            // running max of the block scales (float bits, >= 0)
+  float f[4];                              // power-of-two factor carried by P_j
   float red[4][kHeads];
   float m_used[kHeads];
   float alpha[kHeads];
   float lse_out[kHeads];
   float linv[kHeads];
+  float sc[kTile][4];                      // block scales of the tile's tokens
   unsigned char valid[kTile];
 };
 
-constexpr size_t kSmemBytes = 1024 + kQBytes + kKBytes + sizeof(Misc);
+constexpr size_t kSmemBytes = 1024 + kQBytes + kKBytes + kPAllBytes + sizeof(Misc);
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {  // byte offset in a 128B-swizzled chunk
   return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
-// 4 E4M3 codes * scale -> 4 fp16 (as two f16x2 words).
-__device__ __forceinline__ uint2 dq4(uint32_t w, float sc) {
-  const float2 a = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu)));
-  const float2 c = f16x2_to_f32x2(e4m3x2_to_f16x2((uint16_t)(w >> 16)));
-  return make_uint2(f32x2_to_f16x2_sat(a.x * sc, a.y * sc), f32x2_to_f16x2_sat(c.x * sc, c.y * sc));
+// 4 E4M3 codes -> 4 fp16 (exact).
+__device__ __forceinline__ uint2 codes4(uint32_t w) {
+  return make_uint2(e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w >> 16)));
 }
 
 // 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
@@ -95,24 +110,30 @@ __device__ __forceinline__ uint4 bf8_to_h8(uint4 v, int& range_bad) {
                     bf2_to_h2(v.w, range_bad));
 }
 
-// Warp reduce-scatter over 64 per-thread values: afterwards lane l holds the
-// reduction over the warp's 32 threads for columns 2l and 2l+1.
+__device__ __forceinline__ uint16_t f32_to_f16_sat(float x) {
+  return (uint16_t)(f32x2_to_f16x2_sat(x, 0.f) & 0xFFFFu);
+}
+
+// Warp reduce-scatter over 32 per-thread values: afterwards lane l holds the
+// reduction over the warp's 32 threads of column l.
 template <bool kMax>
-__device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lane) {
-  float a[32];
-  const bool hi16 = lane & 16;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    const float send = hi16 ? v[i] : v[32 + i];
-    const float keep = hi16 ? v[32 + i] : v[i];
-    const float r = __shfl_xor_sync(0xffffffffu, send, 16);
-    a[i] = kMax ? fmaxf(keep, r) : keep + r;
-  }
-#pragma unroll
-  for (int span = 16, x = 8; span >= 2; span >>= 1, x >>= 1) {
-    const bool hi = lane & x;
+__device__ __forceinline__ float reduce_scatter32(const float (&v)[32], int lane) {
+  float a[16];
+  {
+    const bool hi = lane & 16;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
+      const float send = hi ? v[i] : v[16 + i];
+      const float keep = hi ? v[16 + i] : v[i];
+      const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = kMax ? fmaxf(keep, r) : keep + r;
+    }
+  }
+#pragma unroll
+  for (int span = 8, x = 8; span >= 1; span >>= 1, x >>= 1) {
+    const bool hi = lane & x;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
       if (i < span) {
         const float send = hi ? a[i] : a[span + i];
         const float keep = hi ? a[span + i] : a[i];
@@ -121,15 +142,13 @@ __device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lan
       }
     }
   }
-  return make_float2(a[0], a[1]);
+  return a[0];
 }
 
 __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  unsigned char* Qs = base;
-  unsigned char* Ks = base + kQBytes;
-  Misc& ms = *reinterpret_cast<Misc*>(base + kQBytes + kKBytes);
+  Misc& ms = *reinterpret_cast<Misc*>(base + kQBytes + kKBytes + kPAllBytes);
   volatile int* abort = &ms.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -138,6 +157,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const int pos_end = min(pos0 + p.split_len, p.topk_n);
   const int n_tiles = pos_end > pos0 ? (pos_end - pos0 + kTile - 1) / kTile : 0;
   const int hg_valid = min(kHeads, p.H - kHeads * g);
+  const uint32_t q_base = ptx::smem_u32(base);
+  const uint32_t k_base = q_base + kQBytes;
+  const uint32_t p_base = k_base + kKBytes;
 
   if (threadIdx.x == 0) {
     ptx::mbar_init(&ms.q_ready, kGatherThreads);
@@ -152,6 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     ms.need_rescale = 0;
     ms.stop = 0;
     ms.range_err = 0;
+    ms.f_set = 0;
+    for (int j = 0; j < 4; ++j) {
+      ms.scmax[j] = 0;
+      ms.f[j] = 1.f;
+    }
     ptx::fence_mbar_init();
   }
   if (threadIdx.x < kHeads) {
@@ -167,7 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = ms.tmem_slot;
-  const uint32_t q_base = ptx::smem_u32(Qs), k_base = ptx::smem_u32(Ks);
 
   if (n_tiles == 0) {
     // empty partition: out = 0, lse = -inf
@@ -194,11 +220,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           ok = ptx::mbar_wait_bounded(&ms.chunk_ready[c], ph, abort);
           if (!ok) break;
           ptx::tc_fence_after();
+          const uint32_t d_col = kSCol + 32 * (c < 8 ? (c >> 1) : 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t da = ptx::sw128_desc(k_base + c * kKChunkBytes + kk * 32, 16, 1024);
             const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + kk * 32, 16, 1024);
-            ptx::mma_f16_ss(tmem + kSCol, da, db, kIdescQK, (c | kk) != 0);
+            // the first MMA into a block's accumulator (even chunk, first K step) overwrites it
+            ptx::mma_f16_ss(tmem + d_col, da, db, kIdescQK, ((c & 1) | kk) != 0);
           }
         }
         if (!ok) break;
@@ -210,10 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
 #pragma unroll
           for (int kk = 0; kk < kTile / 16; ++kk) {
             const uint64_t da = ptx::sw128_desc(k_base + (2 * j) * kKChunkBytes + kk * 2048, kKChunkBytes, 1024);
-            // P spans one 64-head atom along N, so its leading offset is never stepped; it is set
-            // equal to the stride so that no reading of the two fields leaves the rope chunk.
-            const uint64_t db = ptx::sw128_desc(k_base + 8 * kKChunkBytes + kk * 2048, 1024, 1024);
-            ptx::mma_f16_ss(tmem + 64 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t db =
+                ptx::sw128_desc(p_base + j * kPBytes + (kk >> 2) * kPChunkBytes + (kk & 3) * 32, 16, 1024);
+            ptx::mma_f16_ss(tmem + 32 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
           }
           ptx::mma_commit(&ms.chunk_free[j]);
         }
@@ -225,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
     }
   } else if (warp >= 4) {
-    // ------------------------------------------------------------------ gather + dequantise
+    // ------------------------------------------------------------------ gather + convert
     const int gid = threadIdx.x - 128;
     const int tl = gid >> 1, half = gid & 1;
     const int seq_len = __ldg(p.seq_lens + b);
@@ -233,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     const int32_t* tk_row = p.topk + (size_t)b * p.topk_n;
     int range_bad = 0;
 
-    uint4 lat[16], rope[4], scv;
+    uint4 lat[16], rope[4], scv = make_uint4(0, 0, 0, 0);
     auto load_row = [&](int64_t r) {
       if (r >= 0) {
         const unsigned char* rec = p.kv + r * kRecordBytes;
@@ -249,25 +276,22 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       return pos < pos_end ? __ldg(tk_row + pos) : -1;
     };
 
-    int t_cur = topk_at(0);
+    const int t_cur = topk_at(0);
     // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
     {
       const uint16_t* qg = p.q + ((size_t)b * p.H + (size_t)g * kHeads) * kDQK;
-#pragma unroll 1
-      for (int k0 = 0; k0 < 18; k0 += 6) {
-        uint4 v[6];
+      uint4 v[9];
 #pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const int id = gid + kGatherThreads * (k0 + k);
-          const int n = id / 72, j = id % 72;
-          v[k] = n < hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j) : make_uint4(0, 0, 0, 0);
-        }
+      for (int k = 0; k < 9; ++k) {
+        const int id = gid + kGatherThreads * k;
+        const int n = id / 72, j = id % 72;
+        v[k] = n < hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j) : make_uint4(0, 0, 0, 0);
+      }
 #pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          const int id = gid + kGatherThreads * (k0 + k);
-          const int n = id / 72, j = id % 72;
-          ptx::sts128(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
-        }
+      for (int k = 0; k < 9; ++k) {
+        const int id = gid + kGatherThreads * k;
+        const int n = id / 72, j = id % 72;
+        ptx::sts128(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
       }
     }
     int64_t row = row_of(bt_row, t_cur, seq_len, p.max_pages, p.num_pages, p.err);
@@ -279,19 +303,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int t_next = (i + 1 < n_tiles) ? topk_at(i + 1) : -1;
       const bool valid = row >= 0;
-      float sc[4];
-      sc[0] = __uint_as_float(scv.x); sc[1] = __uint_as_float(scv.y);
-      sc[2] = __uint_as_float(scv.z); sc[3] = __uint_as_float(scv.w);
-      if (valid) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) range_bad |= !(fabsf(sc[k]) * 448.f <= kFp16Max);
-      }
-      // latent chunks: this thread owns units 4c+half and 4c+2+half of chunk c
+      // latent chunks: this thread owns units 4c+half and 4c+2+half (16 dims each) of chunk c
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (i > 0 && !ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort)) { ok = false; break; }
         if (j == 0 && half == 0) {
           ms.valid[tl] = valid;
+          const float s0 = valid ? __uint_as_float(scv.x) : 0.f, s1 = valid ? __uint_as_float(scv.y) : 0.f;
+          const float s2 = valid ? __uint_as_float(scv.z) : 0.f, s3 = valid ? __uint_as_float(scv.w) : 0.f;
+          ms.sc[tl][0] = s0; ms.sc[tl][1] = s1; ms.sc[tl][2] = s2; ms.sc[tl][3] = s3;
+          if (valid) {
+            atomicMax(&ms.scmax[0], __float_as_int(fabsf(s0)));
+            atomicMax(&ms.scmax[1], __float_as_int(fabsf(s1)));
+            atomicMax(&ms.scmax[2], __float_as_int(fabsf(s2)));
+            atomicMax(&ms.scmax[3], __float_as_int(fabsf(s3)));
+          }
           ptx::mbar_arrive(&ms.meta_ready);
         }
 #pragma unroll
@@ -300,12 +326,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int k = 2 * c + e;                  // lat[] index: unit u = 2k + half
-            const int u = 2 * k + half;
-            const int uc = u & 3;                     // 16-dim unit within the chunk
+            const int uc = (2 * k + half) & 3;        // 16-dim unit within the chunk
             uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
             if (valid) {
-              const float s = sc[u >> 3];
-              const uint2 a0 = dq4(lat[k].x, s), a1 = dq4(lat[k].y, s), a2 = dq4(lat[k].z, s), a3 = dq4(lat[k].w, s);
+              const uint2 a0 = codes4(lat[k].x), a1 = codes4(lat[k].y), a2 = codes4(lat[k].z), a3 = codes4(lat[k].w);
               lo = make_uint4(a0.x, a0.y, a1.x, a1.y);
               hi = make_uint4(a2.x, a2.y, a3.x, a3.y);
             }
@@ -318,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         }
       }
       if (!ok) break;
-      // rope chunk (it holds the previous tile's P until that tile's PV is done)
+      // rope chunk: free once the previous tile's PV is done (all of its MMAs have completed)
       if (i > 0 && !ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort)) { ok = false; break; }
       {
         const uint32_t cb = k_base + 8 * kKChunkBytes;
@@ -338,55 +362,66 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     if (range_bad) ms.range_err = 1;
   } else {
     // ------------------------------------------------------------------ softmax + epilogue (warps 0..3)
-    const int t = threadIdx.x;                    // TMEM lane = token within the tile / dim within a block
-    const float c2 = p.sm_scale * 1.4426950408889634f;
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    float lsum0 = 0.f, lsum1 = 0.f;               // this warp's sums for heads 2*lane, 2*lane+1
     // Every softmax warp runs the same sequence of named barriers; a failed wait
     // only stops the loop through ms.stop, which warp 0 publishes between the
     // two barriers of a tile, so all four warps leave at the same tile.
+    const int t = threadIdx.x;                    // TMEM lane = token within the tile / dim within a block
+    const float c2 = p.sm_scale * 1.4426950408889634f;
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    float lsum = 0.f;                             // this warp's sum for head `lane`
+    int range_bad = 0;
     bool ok = true;
     for (int i = 0; i < n_tiles; ++i) {
       const uint32_t ph = i & 1;
       ok = ptx::mbar_wait_bounded(&ms.meta_ready, ph, abort) && ptx::mbar_wait_bounded(&ms.s_full, ph, abort);
       ptx::tc_fence_after();
-      float s[64];
+      const float scb[4] = {ms.sc[t][0], ms.sc[t][1], ms.sc[t][2], ms.sc[t][3]};
+      float s[32];
       {
         uint32_t r[32];
-        ptx::tmem_ld32(tmem + lane_base + kSCol, r);
+        ptx::tmem_ld32(tmem + lane_base + kSCol + 128, r);   // rope accumulator
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < 32; ++h) s[h] = __uint_as_float(r[h]);
-        ptx::tmem_ld32(tmem + lane_base + kSCol + 32, r);
-        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s[32 + h] = __uint_as_float(r[h]);
+        for (int bb = 0; bb < 4; ++bb) {
+          ptx::tmem_ld32(tmem + lane_base + kSCol + 32 * bb, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s[h] = fmaf(scb[bb], __uint_as_float(r[h]), s[h]);
+        }
       }
       const bool valid = ms.valid[t];
 #pragma unroll
-      for (int h = 0; h < 64; ++h) s[h] = valid ? s[h] * c2 : -CUDART_INF_F;
-      const float2 mx = reduce_scatter64<true>(s, lane);
-      ms.red[warp][2 * lane] = mx.x;
-      ms.red[warp][2 * lane + 1] = mx.y;
+      for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * c2 : -CUDART_INF_F;
+      const float mx = reduce_scatter32<true>(s, lane);
+      ms.red[warp][lane] = mx;
       ptx::named_bar_sync(1, kSoftmaxThreads);
       if (warp == 0) {
+        const int h = lane;
+        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+        const float mo = ms.m_used[h];
+        float mn = mo, a = 1.f;
         bool resc = false;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
-          const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-          const float mo = ms.m_used[h];
-          float mn = mo, a = 1.f;
-          if (mt > mo + kRescaleThreshold) {      // also true when mo = -inf and mt is finite
-            mn = mt;
-            a = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
-            resc |= (mo != -CUDART_INF_F);
-          }
-          ms.m_used[h] = mn;
-          ms.alpha[h] = a;
+        if (mt > mo + kRescaleThreshold) {        // also true when mo = -inf and mt is finite
+          mn = mt;
+          a = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
+          resc = (mo != -CUDART_INF_F);
         }
+        ms.m_used[h] = mn;
+        ms.alpha[h] = a;
         const bool any = __any_sync(0xffffffffu, resc);
+        // P_j factor: fixed at the first tile that holds data, so that F_j * max scale is in [0.5, 1)
+        const bool set_now = !ms.f_set && (ms.scmax[0] | ms.scmax[1] | ms.scmax[2] | ms.scmax[3]) != 0;
+        if (set_now && lane < 4) {
+          const float mxs = __int_as_float(ms.scmax[lane]);
+          int e = 0;
+          if (mxs > 0.f) frexpf(mxs, &e);
+          ms.f[lane] = ldexpf(1.f, -e);
+        }
+        __syncwarp();
         if (lane == 0) {
+          if (set_now) ms.f_set = 1;
           ms.need_rescale = any && i > 0;
           ms.stop = *abort;
         }
@@ -396,41 +431,36 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         ok = false;
         break;
       }
-      // P row for this token: 64 heads fp16 (128 B), 128B-swizzled over the rope chunk
-      float pv[64];
+      float pv[32];
+#pragma unroll
+      for (int h = 0; h < 32; ++h) {
+        const float m = ms.m_used[h];
+        pv[h] = (m == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m);
+      }
+      // P_j[h][t] = p * scale_j * F_j, K-major (rows = heads, 2 chunks of 64 tokens)
       {
-        const uint32_t cb = k_base + 8 * kKChunkBytes;
+        const uint32_t tok_off = (t >> 6) * kPChunkBytes + (t & 7) * 2;
+        const uint32_t unit = (t & 63) >> 3;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          uint32_t w[4];
+        for (int j = 0; j < 4; ++j) {
+          const float f = scb[j] * ms.f[j];
+          range_bad |= !(f * 256.f <= kFp16Max);
+          unsigned char* pj = base + kQBytes + kKBytes + j * kPBytes + tok_off;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int h = 8 * u + 2 * q;
-            const float m0 = ms.m_used[h], m1 = ms.m_used[h + 1];
-            const float p0 = (m0 == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m0);
-            const float p1 = (m1 == -CUDART_INF_F) ? 0.f : exp2f(s[h + 1] - m1);
-            pv[h] = p0;
-            pv[h + 1] = p1;
-            w[q] = f32x2_to_f16x2_sat(p0, p1);
-          }
-          ptx::sts128(cb + swz(t, u), make_uint4(w[0], w[1], w[2], w[3]));
+          for (int h = 0; h < 32; ++h) *reinterpret_cast<uint16_t*>(pj + swz(h, unit)) = f32_to_f16_sat(pv[h] * f);
         }
       }
-      const float2 ps = reduce_scatter64<false>(pv, lane);
-      lsum0 = lsum0 * ms.alpha[2 * lane] + ps.x;
-      lsum1 = lsum1 * ms.alpha[2 * lane + 1] + ps.y;
+      const float ps = reduce_scatter32<false>(pv, lane);
+      lsum = lsum * ms.alpha[lane] + ps;
       if (ms.need_rescale) {
         for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          const uint32_t ta = tmem + lane_base + 32 * j;
+          ptx::tmem_ld32(ta, r);
+          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t r[32];
-            const uint32_t ta = tmem + lane_base + 64 * j + 32 * hh;
-            ptx::tmem_ld32(ta, r);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * ms.alpha[32 * hh + q]);
-            ptx::tmem_st32(ta, r);
-          }
+          for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * ms.alpha[q]);
+          ptx::tmem_st32(ta, r);
         }
         ptx::tmem_wait_st();
       }
@@ -438,41 +468,35 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       ptx::fence_proxy_async_smem();
       ptx::mbar_arrive(&ms.p_ready);
     }
-    // epilogue: O / l, lse
+    if (range_bad) ms.range_err = 1;
+    // epilogue: O / (l F_j), lse
     if (ok) ok = ptx::mbar_wait_bounded(&ms.pv_done, (n_tiles - 1) & 1, abort);
     ptx::tc_fence_after();
-    ms.red[warp][2 * lane] = lsum0;
-    ms.red[warp][2 * lane + 1] = lsum1;
+    ms.red[warp][lane] = lsum;
     ptx::named_bar_sync(1, kSoftmaxThreads);
     if (warp == 0) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int h = 2 * lane + e;
-        const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
-        ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
-        ms.lse_out[h] = L > 0.f ? (ms.m_used[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
-      }
+      const int h = lane;
+      const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+      ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
+      ms.lse_out[h] = L > 0.f ? (ms.m_used[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
     }
     ptx::named_bar_sync(2, kSoftmaxThreads);
     if (ok) {
       for (int j = 0; j < 4; ++j) {
         const int d = 128 * j + t;
+        const float finv = 1.f / ms.f[j];
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem + lane_base + 32 * j, r);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          ptx::tmem_ld32(tmem + lane_base + 64 * j + 32 * hh, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const int hl = 32 * hh + q;
-            if (hl < hg_valid) {
-              const float o = __uint_as_float(r[q]) * ms.linv[hl];
-              const size_t h = (size_t)g * kHeads + hl;
-              if (p.final_out) {
-                p.out[((size_t)b * p.H + h) * kDLatent + d] = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
-              } else {
-                p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = o;
-              }
+        for (int q = 0; q < 32; ++q) {
+          if (q < hg_valid) {
+            const float o = __uint_as_float(r[q]) * (ms.linv[q] * finv);
+            const size_t h = (size_t)g * kHeads + q;
+            if (p.final_out) {
+              p.out[((size_t)b * p.H + h) * kDLatent + d] = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
+            } else {
+              p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = o;
             }
           }
         }
@@ -500,6 +524,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
 bool split_shape_supported(int H, int topk) {
   return (H == 16 || H == 32 || H == 64 || H == 128) && topk >= 1 && topk <= kMaxTopk;
 }
+
+int split_heads_per_cta() { return kHeads; }
 
 int split_ctas_per_sm(int H) {
   (void)H;
