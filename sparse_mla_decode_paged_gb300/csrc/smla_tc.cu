@@ -57,6 +57,8 @@ constexpr int kPAllBytes = 4 * kPBytes;                  // 32768
 constexpr int kThreads = 416;
 constexpr int kSoftmaxThreads = 128;       // warps 0..3 (TMEM lane quadrants 0..3)
 constexpr int kGatherThreads = 256;        // warps 4..11
+constexpr int kGatherWarps = kGatherThreads / 32;
+constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
 constexpr int kMmaWarp = 12;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 128;            // S_b at kSCol + 32 b, b = 0..4 (4 = rope)
@@ -162,13 +164,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const uint32_t p_base = k_base + kKBytes;
 
   if (threadIdx.x == 0) {
-    ptx::mbar_init(&ms.q_ready, kGatherThreads);
-    ptx::mbar_init(&ms.meta_ready, kTile);
+    // producer barriers count one arrival per warp (lane 0 after the warp's fences)
+    ptx::mbar_init(&ms.q_ready, kGatherWarps);
+    ptx::mbar_init(&ms.meta_ready, kGatherWarps);
     ptx::mbar_init(&ms.s_full, 1);
-    ptx::mbar_init(&ms.p_ready, kSoftmaxThreads);
+    ptx::mbar_init(&ms.p_ready, kSoftmaxWarps);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
-    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&ms.chunk_ready[c], kGatherThreads);
+    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&ms.chunk_ready[c], kGatherWarps);
     for (int j = 0; j < 4; ++j) ptx::mbar_init(&ms.chunk_free[j], 1);
     ms.abort = 0;
     ms.need_rescale = 0;
@@ -297,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     int64_t row = row_of(bt_row, t_cur, seq_len, p.max_pages, p.num_pages, p.err);
     load_row(row);
     ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive(&ms.q_ready);
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms.q_ready);
 
     bool ok = true;
     for (int i = 0; ok && i < n_tiles; ++i) {
@@ -306,19 +310,31 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       // latent chunks: this thread owns units 4c+half and 4c+2+half (16 dims each) of chunk c
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (i > 0 && !ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort)) { ok = false; break; }
-        if (j == 0 && half == 0) {
-          ms.valid[tl] = valid;
-          const float s0 = valid ? __uint_as_float(scv.x) : 0.f, s1 = valid ? __uint_as_float(scv.y) : 0.f;
-          const float s2 = valid ? __uint_as_float(scv.z) : 0.f, s3 = valid ? __uint_as_float(scv.w) : 0.f;
-          ms.sc[tl][0] = s0; ms.sc[tl][1] = s1; ms.sc[tl][2] = s2; ms.sc[tl][3] = s3;
-          if (valid) {
-            atomicMax(&ms.scmax[0], __float_as_int(fabsf(s0)));
-            atomicMax(&ms.scmax[1], __float_as_int(fabsf(s1)));
-            atomicMax(&ms.scmax[2], __float_as_int(fabsf(s2)));
-            atomicMax(&ms.scmax[3], __float_as_int(fabsf(s3)));
+        if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        if (j == 0) {
+          float sv[4] = {valid ? __uint_as_float(scv.x) : 0.f, valid ? __uint_as_float(scv.y) : 0.f,
+                         valid ? __uint_as_float(scv.z) : 0.f, valid ? __uint_as_float(scv.w) : 0.f};
+          if (half == 0) {
+            ms.valid[tl] = valid;
+            ms.sc[tl][0] = sv[0]; ms.sc[tl][1] = sv[1]; ms.sc[tl][2] = sv[2]; ms.sc[tl][3] = sv[3];
           }
-          ptx::mbar_arrive(&ms.meta_ready);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float m = fabsf(sv[q]);
+#pragma unroll
+            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            sv[q] = m;
+          }
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (sv[q] > 0.f) atomicMax(&ms.scmax[q], __float_as_int(sv[q]));
+            ptx::mbar_arrive(&ms.meta_ready);
+          }
         }
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -338,12 +354,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
             ptx::sts128(cb + swz(tl, 2 * uc + 1), hi);
           }
           ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(&ms.chunk_ready[c]);
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&ms.chunk_ready[c]);
         }
       }
       if (!ok) break;
       // rope chunk: free once the previous tile's PV is done (all of its MMAs have completed)
-      if (i > 0 && !ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort)) { ok = false; break; }
+      if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
       {
         const uint32_t cb = k_base + 8 * kKChunkBytes;
 #pragma unroll
@@ -352,7 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           ptx::sts128(cb + swz(tl, r), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
         }
         ptx::fence_proxy_async_smem();
-        ptx::mbar_arrive(&ms.chunk_ready[8]);
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.chunk_ready[8]);
       }
       if (i + 1 < n_tiles) {
         row = row_of(bt_row, t_next, seq_len, p.max_pages, p.num_pages, p.err);
@@ -374,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     for (int i = 0; i < n_tiles; ++i) {
       const uint32_t ph = i & 1;
       ok = ptx::mbar_wait_bounded(&ms.meta_ready, ph, abort) && ptx::mbar_wait_bounded(&ms.s_full, ph, abort);
+      ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
       const float scb[4] = {ms.sc[t][0], ms.sc[t][1], ms.sc[t][2], ms.sc[t][3]};
       float s[32];
@@ -466,11 +488,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       }
       ptx::tc_fence_before();
       ptx::fence_proxy_async_smem();
-      ptx::mbar_arrive(&ms.p_ready);
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms.p_ready);
     }
     if (range_bad) ms.range_err = 1;
     // epilogue: O / (l F_j), lse
     if (ok) ok = ptx::mbar_wait_bounded(&ms.pv_done, (n_tiles - 1) & 1, abort);
+    ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
     ms.red[warp][lane] = lsum;
     ptx::named_bar_sync(1, kSoftmaxThreads);
