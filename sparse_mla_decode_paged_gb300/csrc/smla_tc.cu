@@ -11,13 +11,14 @@
 //                      (9 chunks of 64 dims); the four fp32 scales of each
 //                      token go to shared memory.  The next tile's loads are
 //                      issued as soon as a tile is stored.
-//   MMA warp (1 lane)  QK per scale block: S_b^T[128 tok x 32 heads] =
+//   MMA (warp 0 lane 0) QK per scale block: S_b^T[128 tok x 32 heads] =
 //                      K_b . Q_b^T for the four 128-dim latent blocks and the
 //                      rope (a3), M=128 N=32, five fp32 TMEM accumulators;
 //                      then O_j^T[128 dims x 32 heads] += V_j^T . P_j^T for the
 //                      four dim blocks (a5), V_j^T being the same codes read
 //                      MN-major and P_j = P scaled by the tokens' block-j scale.
-//   softmax warps (4)  one TMEM lane (token) per thread: exact score
+//   softmax warps (4)  load Q once (fp16, swizzled); then one TMEM lane
+//                      (token) per thread: exact score
 //                      s = sum_b scale_b S_b + S_rope in fp32; per-head
 //                      running max over the tile (warp reduce-scatter + shared
 //                      memory), P = exp2(s - m) (a4), the four scaled P_j in
@@ -30,9 +31,13 @@
 // of two F_j (fixed at the first tile with data) so that it sits in the fp16
 // normal range; the epilogue divides it out.
 //
+// QK of a tile, its softmax and its PV are sequential (one K tile), so the
+// MMAs are issued by lane 0 of the first softmax warp between its softmax
+// steps; no warp is spent on issue only.
+//
 // Shared memory: Q 36 KB (32 heads x 576 fp16) + K tile 144 KB (128 x 576
 // fp16) + P 32 KB (4 x 32 heads x 128 tokens fp16) + barriers: one CTA per
-// SM, 13 warps.  TMEM: O^T in columns 0..127, S in 128..287 (512 allocated).
+// SM, 12 warps.  TMEM: O^T in columns 0..127, S in 128..287 (512 allocated).
 // Sources: "The 64-Block Barrier" ("The Smoking Gun", "The Split-K
 // Prescription"); "Inside the Decode Performance Investigation" (Task 1).
 #include <cuda_runtime.h>
@@ -54,12 +59,12 @@ constexpr int kPBytes = 2 * kPChunkBytes;                // one P_j: 2 chunks of
 constexpr int kQBytes = kChunks * kQChunkBytes;          // 36864
 constexpr int kKBytes = kChunks * kKChunkBytes;          // 147456
 constexpr int kPAllBytes = 4 * kPBytes;                  // 32768
-constexpr int kThreads = 416;
-constexpr int kSoftmaxThreads = 128;       // warps 0..3 (TMEM lane quadrants 0..3)
+// 12 warps = 3 per SM sub-partition, which leaves 168 registers per thread.
+constexpr int kThreads = 384;
+constexpr int kSoftmaxThreads = 128;       // warps 0..3 (TMEM lane quadrants 0..3); lane 0 of warp 0 issues MMAs
 constexpr int kGatherThreads = 256;        // warps 4..11
 constexpr int kGatherWarps = kGatherThreads / 32;
 constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
-constexpr int kMmaWarp = 12;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 128;            // S_b at kSCol + 32 b, b = 0..4 (4 = rope)
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
@@ -70,7 +75,7 @@ constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 0);
 
 struct Misc {
   uint64_t q_ready, meta_ready, s_full, p_ready, pv_done, teardown;
-  uint64_t chunk_ready[kChunks];
+  uint64_t kv_ready[5];                    // latent blocks 0..3 (two chunks each), rope
   uint64_t chunk_free[4];
   uint32_t tmem_slot;
   int abort;
@@ -163,15 +168,30 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const uint32_t k_base = q_base + kQBytes;
   const uint32_t p_base = k_base + kKBytes;
 
+  if (n_tiles == 0) {
+    // empty partition: out = 0, lse = -inf
+    for (int i = threadIdx.x; i < hg_valid * kDLatent; i += kThreads) {
+      const int h = g * kHeads + i / kDLatent, d = i % kDLatent;
+      if (p.final_out) p.out[((size_t)b * p.H + h) * kDLatent + d] = 0;
+      else p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = 0.f;
+    }
+    if (threadIdx.x < hg_valid) {
+      const int h = g * kHeads + threadIdx.x;
+      if (p.final_out) p.lse[(size_t)b * p.H + h] = -CUDART_INF_F;
+      else p.lse_part[((size_t)b * p.nsplit + split) * p.H + h] = -CUDART_INF_F;
+    }
+    return;
+  }
+
   if (threadIdx.x == 0) {
     // producer barriers count one arrival per warp (lane 0 after the warp's fences)
-    ptx::mbar_init(&ms.q_ready, kGatherWarps);
+    ptx::mbar_init(&ms.q_ready, kSoftmaxWarps);
     ptx::mbar_init(&ms.meta_ready, kGatherWarps);
     ptx::mbar_init(&ms.s_full, 1);
     ptx::mbar_init(&ms.p_ready, kSoftmaxWarps);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
-    for (int c = 0; c < kChunks; ++c) ptx::mbar_init(&ms.chunk_ready[c], kGatherWarps);
+    for (int c = 0; c < 5; ++c) ptx::mbar_init(&ms.kv_ready[c], kGatherWarps);
     for (int j = 0; j < 4; ++j) ptx::mbar_init(&ms.chunk_free[j], 1);
     ms.abort = 0;
     ms.need_rescale = 0;
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     ms.m_used[threadIdx.x] = -CUDART_INF_F;
     ms.alpha[threadIdx.x] = 1.f;
   }
-  if (warp == kMmaWarp && n_tiles > 0) {
+  if (warp == 0) {
     ptx::tmem_alloc(&ms.tmem_slot, kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -198,65 +218,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   ptx::tc_fence_after();
   const uint32_t tmem = ms.tmem_slot;
 
-  if (n_tiles == 0) {
-    // empty partition: out = 0, lse = -inf
-    for (int i = threadIdx.x; i < hg_valid * kDLatent; i += kThreads) {
-      const int h = g * kHeads + i / kDLatent, d = i % kDLatent;
-      if (p.final_out) p.out[((size_t)b * p.H + h) * kDLatent + d] = 0;
-      else p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = 0.f;
-    }
-    if (threadIdx.x < hg_valid) {
-      const int h = g * kHeads + threadIdx.x;
-      if (p.final_out) p.lse[(size_t)b * p.H + h] = -CUDART_INF_F;
-      else p.lse_part[((size_t)b * p.nsplit + split) * p.H + h] = -CUDART_INF_F;
-    }
-    return;
-  }
-
-  if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = ptx::mbar_wait_bounded(&ms.q_ready, 0, abort);
-      for (int i = 0; ok && i < n_tiles; ++i) {
-        const uint32_t ph = i & 1;
-        for (int c = 0; ok && c < kChunks; ++c) {
-          ok = ptx::mbar_wait_bounded(&ms.chunk_ready[c], ph, abort);
-          if (!ok) break;
-          ptx::tc_fence_after();
-          const uint32_t d_col = kSCol + 32 * (c < 8 ? (c >> 1) : 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t da = ptx::sw128_desc(k_base + c * kKChunkBytes + kk * 32, 16, 1024);
-            const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + kk * 32, 16, 1024);
-            // the first MMA into a block's accumulator (even chunk, first K step) overwrites it
-            ptx::mma_f16_ss(tmem + d_col, da, db, kIdescQK, ((c & 1) | kk) != 0);
-          }
-        }
-        if (!ok) break;
-        ptx::mma_commit(&ms.s_full);
-        ok = ptx::mbar_wait_bounded(&ms.p_ready, ph, abort);
-        if (!ok) break;
-        ptx::tc_fence_after();
-        for (int j = 0; j < 4; ++j) {
-#pragma unroll
-          for (int kk = 0; kk < kTile / 16; ++kk) {
-            const uint64_t da = ptx::sw128_desc(k_base + (2 * j) * kKChunkBytes + kk * 2048, kKChunkBytes, 1024);
-            const uint64_t db =
-                ptx::sw128_desc(p_base + j * kPBytes + (kk >> 2) * kPChunkBytes + (kk & 3) * 32, 16, 1024);
-            ptx::mma_f16_ss(tmem + 32 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-          }
-          ptx::mma_commit(&ms.chunk_free[j]);
-        }
-        ptx::mma_commit(&ms.pv_done);
-      }
-      // drain every MMA this thread issued before the TMEM is released (time limit only)
-      ptx::mma_commit(&ms.teardown);
-      volatile int no_abort = 0;
-      ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
-    }
-  } else if (warp >= 4) {
+  if (warp >= 4) {
     // ------------------------------------------------------------------ gather + convert
-    const int gid = threadIdx.x - 128;
+    const int gid = threadIdx.x - kSoftmaxThreads;
     const int tl = gid >> 1, half = gid & 1;
     const int seq_len = __ldg(p.seq_lens + b);
     const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
@@ -279,35 +243,14 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       return pos < pos_end ? __ldg(tk_row + pos) : -1;
     };
 
-    const int t_cur = topk_at(0);
-    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
-    {
-      const uint16_t* qg = p.q + ((size_t)b * p.H + (size_t)g * kHeads) * kDQK;
-      uint4 v[9];
-#pragma unroll
-      for (int k = 0; k < 9; ++k) {
-        const int id = gid + kGatherThreads * k;
-        const int n = id / 72, j = id % 72;
-        v[k] = n < hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int k = 0; k < 9; ++k) {
-        const int id = gid + kGatherThreads * k;
-        const int n = id / 72, j = id % 72;
-        ptx::sts128(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
-      }
-    }
-    int64_t row = row_of(bt_row, t_cur, seq_len, p.max_pages, p.num_pages, p.err);
+    int64_t row = row_of(bt_row, topk_at(0), seq_len, p.max_pages, p.num_pages, p.err);
     load_row(row);
-    ptx::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ms.q_ready);
 
     bool ok = true;
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int t_next = (i + 1 < n_tiles) ? topk_at(i + 1) : -1;
       const bool valid = row >= 0;
-      // latent chunks: this thread owns units 4c+half and 4c+2+half (16 dims each) of chunk c
+      // latent block j = chunks 2j, 2j+1; this thread owns units 4c+half and 4c+2+half of chunk c
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort))) {
@@ -353,10 +296,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
             ptx::sts128(cb + swz(tl, 2 * uc), lo);
             ptx::sts128(cb + swz(tl, 2 * uc + 1), hi);
           }
-          ptx::fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&ms.chunk_ready[c]);
         }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[j]);
       }
       if (!ok) break;
       // rope chunk: free once the previous tile's PV is done (all of its MMAs have completed)
@@ -373,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.chunk_ready[8]);
+        if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
       }
       if (i + 1 < n_tiles) {
         row = row_of(bt_row, t_next, seq_len, p.max_pages, p.num_pages, p.err);
@@ -382,18 +325,64 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     }
     if (range_bad) ms.range_err = 1;
   } else {
-    // ------------------------------------------------------------------ softmax + epilogue (warps 0..3)
+    // ------------------------------------------------------------------ Q, MMA issue, softmax, epilogue
     // Every softmax warp runs the same sequence of named barriers; a failed wait
     // only stops the loop through ms.stop, which warp 0 publishes between the
     // two barriers of a tile, so all four warps leave at the same tile.
     const int t = threadIdx.x;                    // TMEM lane = token within the tile / dim within a block
+    const bool issuer = (threadIdx.x == 0);
+    int range_bad = 0;
+    {
+      // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
+      const uint16_t* qg = p.q + ((size_t)b * p.H + (size_t)g * kHeads) * kDQK;
+#pragma unroll 1
+      for (int k0 = 0; k0 < 18; k0 += 9) {
+        uint4 v[9];
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int id = t + kSoftmaxThreads * (k0 + k);
+          const int n = id / 72, j = id % 72;
+          v[k] = n < hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int k = 0; k < 9; ++k) {
+          const int id = t + kSoftmaxThreads * (k0 + k);
+          const int n = id / 72, j = id % 72;
+          ptx::sts128(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
+        }
+      }
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms.q_ready);
+    }
     const float c2 = p.sm_scale * 1.4426950408889634f;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     float lsum = 0.f;                             // this warp's sum for head `lane`
-    int range_bad = 0;
     bool ok = true;
+    bool mma_ok = true;                           // issuer only
+    if (issuer) mma_ok = ptx::mbar_wait_bounded(&ms.q_ready, 0, abort);
     for (int i = 0; i < n_tiles; ++i) {
       const uint32_t ph = i & 1;
+      if (issuer && mma_ok) {
+        // QK: latent block j (chunks 2j, 2j+1) into S_j, then the rope chunk into S_4
+        for (int j = 0; mma_ok && j < 5; ++j) {
+          mma_ok = ptx::mbar_wait_bounded(&ms.kv_ready[j], ph, abort);
+          if (!mma_ok) break;
+          ptx::tc_fence_after();
+          const int c0 = j < 4 ? 2 * j : 8, nc = j < 4 ? 2 : 1;
+          for (int cc = 0; cc < nc; ++cc) {
+            const int c = c0 + cc;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t da = ptx::sw128_desc(k_base + c * kKChunkBytes + kk * 32, 16, 1024);
+              const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + kk * 32, 16, 1024);
+              // the first MMA into a block's accumulator overwrites it
+              ptx::mma_f16_ss(tmem + kSCol + 32 * j, da, db, kIdescQK, (cc | kk) != 0);
+            }
+          }
+        }
+        if (mma_ok) ptx::mma_commit(&ms.s_full);
+      }
       ok = ptx::mbar_wait_bounded(&ms.meta_ready, ph, abort) && ptx::mbar_wait_bounded(&ms.s_full, ph, abort);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
@@ -445,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         if (lane == 0) {
           if (set_now) ms.f_set = 1;
           ms.need_rescale = any && i > 0;
-          ms.stop = *abort;
+          ms.stop = *abort || !ok;
         }
       }
       ptx::named_bar_sync(2, kSoftmaxThreads);
@@ -453,11 +442,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         ok = false;
         break;
       }
-      float pv[32];
+      // P = exp2(s - m), in place
 #pragma unroll
       for (int h = 0; h < 32; ++h) {
         const float m = ms.m_used[h];
-        pv[h] = (m == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m);
+        s[h] = (m == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m);
       }
       // P_j[h][t] = p * scale_j * F_j, K-major (rows = heads, 2 chunks of 64 tokens)
       {
@@ -469,10 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           range_bad |= !(f * 256.f <= kFp16Max);
           unsigned char* pj = base + kQBytes + kKBytes + j * kPBytes + tok_off;
 #pragma unroll
-          for (int h = 0; h < 32; ++h) *reinterpret_cast<uint16_t*>(pj + swz(h, unit)) = f32_to_f16_sat(pv[h] * f);
+          for (int h = 0; h < 32; ++h) *reinterpret_cast<uint16_t*>(pj + swz(h, unit)) = f32_to_f16_sat(s[h] * f);
         }
       }
-      const float ps = reduce_scatter32<false>(pv, lane);
+      const float ps = reduce_scatter32<false>(s, lane);
       lsum = lsum * ms.alpha[lane] + ps;
       if (ms.need_rescale) {
         for (int j = 0; j < 4; ++j) {
@@ -490,6 +479,25 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ms.p_ready);
+      if (issuer && mma_ok) {
+        // PV: O_j^T += V_j^T . P_j^T for the four 128-dim blocks
+        mma_ok = ptx::mbar_wait_bounded(&ms.p_ready, ph, abort);
+        if (mma_ok) {
+          ptx::tc_fence_after();
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int kk = 0; kk < kTile / 16; ++kk) {
+              const uint64_t da = ptx::sw128_desc(k_base + (2 * j) * kKChunkBytes + kk * 2048, kKChunkBytes, 1024);
+              const uint64_t db =
+                  ptx::sw128_desc(p_base + j * kPBytes + (kk >> 2) * kPChunkBytes + (kk & 3) * 32, 16, 1024);
+              ptx::mma_f16_ss(tmem + 32 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(&ms.chunk_free[j]);
+          }
+          ptx::mma_commit(&ms.pv_done);
+        }
+      }
+      __syncwarp();
     }
     if (range_bad) ms.range_err = 1;
     // epilogue: O / (l F_j), lse
@@ -531,6 +539,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         else p.lse_part[((size_t)b * p.nsplit + split) * p.H + h] = ms.lse_out[t];
       }
     }
+    if (issuer) {
+      // drain every MMA issued before the TMEM is released (time limit only)
+      ptx::mma_commit(&ms.teardown);
+      volatile int no_abort = 0;
+      ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
+      if (!mma_ok) *abort = 1;
+    }
   }
 
   ptx::tc_fence_before();
@@ -540,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     if (ms.abort) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
     if (ms.range_err) atomicOr(p.err, SMLA_DEVERR_RANGE);
   }
-  if (warp == kMmaWarp) ptx::tmem_dealloc(tmem, kTmemCols);
+  if (warp == 0) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
