@@ -1,43 +1,39 @@
 // Tensor-core split kernel (sm_103a): tcgen05 MMAs with TMEM accumulators.
 //
-// One CTA per (partition s of the top-k list, group of 32 heads, query b).
+// One CTA per (partition s of the top-k list, group of 64 heads, query b).
 // The partition is walked in tiles of 128 top-k entries:
 //
 //   gather warps (8)   index -> row through the block table (a1); 16-byte
-//                      streaming loads of each 656-byte record into
-//                      registers; the E4M3 latent codes are converted to fp16
-//                      exactly (every E4M3 value is an fp16 value) and the bf16
-//                      rope to fp16 (a2), stored 128B-swizzled into the K tile
-//                      (9 chunks of 64 dims); the four fp32 scales of each
-//                      token go to shared memory.  The next tile's loads are
-//                      issued as soon as a tile is stored.
-//   MMA (warp 0 lane 0) QK per scale block: S_b^T[128 tok x 32 heads] =
-//                      K_b . Q_b^T for the four 128-dim latent blocks and the
-//                      rope (a3), M=128 N=32, five fp32 TMEM accumulators;
-//                      then O_j^T[128 dims x 32 heads] += V_j^T . P_j^T for the
-//                      four dim blocks (a5), V_j^T being the same codes read
-//                      MN-major and P_j = P scaled by the tokens' block-j scale.
+//                      loads of each 656-byte record into registers (warp w
+//                      owns the 32 tokens of TMEM lane quadrant w % 4 and one
+//                      half of the latent dims); dequantisation (a2):
+//                      k = e4m3(code) * scale in fp32, split as
+//                      k = K_hi + K_lo with K_hi = fp16(k) stored 128B-swizzled
+//                      into the K tile (9 chunks of 64 dims) and
+//                      K_lo = fp16(k - K_hi) written into TMEM; bf16 rope to
+//                      fp16 (exact).  The next tile's loads follow at once.
+//   MMA (warp 0 lane 0) S^T[128 tok x 64 heads] = K_hi . Q^T from shared
+//                      memory (36 MMAs M=128 N=64 K=16) plus the correction
+//                      K_lo . Q^T with the A operand read from TMEM (two
+//                      passes of 256 dims), so that the scores carry about
+//                      2^-22 relative error (a3); then
+//                      O^T[512 x 64] += V^T . P^T for the four 128-dim blocks
+//                      (a5), V^T being the latent K_hi read MN-major.
 //   softmax warps (4)  load Q once (fp16, swizzled); then one TMEM lane
-//                      (token) per thread: exact score
-//                      s = sum_b scale_b S_b + S_rope in fp32; per-head
-//                      running max over the tile (warp reduce-scatter + shared
-//                      memory), P = exp2(s - m) (a4), the four scaled P_j in
-//                      fp16, lazy rescale of O when a head's max grows by more
-//                      than 2^8, and the epilogue (a6): O / l and lse.
-//
-// Keeping the latent codes unscaled makes every product in QK exact, so the
-// scores carry fp32 accumulation error only; the per-block scales enter in
-// fp32 in the softmax and, for PV, through P_j.  P_j carries a per-CTA power
-// of two F_j (fixed at the first tile with data) so that it sits in the fp16
-// normal range; the epilogue divides it out.
+//                      (token) per thread: per-head running max over the tile
+//                      (warp reduce-scatter + shared memory), P = exp2(s - m)
+//                      in fp16 written over the rope chunk (a4), lazy rescale
+//                      of O when a head's max grows by more than 2^8, and the
+//                      epilogue (a6): O / l and lse.
 //
 // QK of a tile, its softmax and its PV are sequential (one K tile), so the
 // MMAs are issued by lane 0 of the first softmax warp between its softmax
 // steps; no warp is spent on issue only.
 //
-// Shared memory: Q 36 KB (32 heads x 576 fp16) + K tile 144 KB (128 x 576
-// fp16) + P 32 KB (4 x 32 heads x 128 tokens fp16) + barriers: one CTA per
-// SM, 12 warps.  TMEM: O^T in columns 0..127, S in 128..287 (512 allocated).
+// Shared memory: Q 72 KB (64 heads x 576 fp16) + K tile 144 KB (128 x 576
+// fp16) + barriers: one CTA per SM, 12 warps (3 per SM sub-partition, 168
+// registers per thread).  TMEM: O^T in columns 0..255, S^T in 256..319, K_lo
+// in 320..447 (512 allocated).
 // Sources: "The 64-Block Barrier" ("The Smoking Gun", "The Split-K
 // Prescription"); "Inside the Decode Performance Investigation" (Task 1).
 #include <cuda_runtime.h>
@@ -50,59 +46,56 @@ namespace smla {
 namespace {
 
 constexpr int kTile = 128;                 // top-k entries per tile (MMA M)
-constexpr int kHeads = 32;                 // heads per CTA (MMA N), zero rows past the valid heads
+constexpr int kHeads = 64;                 // heads per CTA (MMA N), zero rows past the valid heads
 constexpr int kChunks = 9;                 // 576 dims / 64
-constexpr int kQChunkBytes = kHeads * 128;               // 4 KB
+constexpr int kQChunkBytes = kHeads * 128;               // 8 KB
 constexpr int kKChunkBytes = kTile * 128;                // 16 KB
-constexpr int kPChunkBytes = kHeads * 128;               // 32 heads x 64 tokens
-constexpr int kPBytes = 2 * kPChunkBytes;                // one P_j: 2 chunks of 64 tokens
-constexpr int kQBytes = kChunks * kQChunkBytes;          // 36864
+constexpr int kQBytes = kChunks * kQChunkBytes;          // 73728
 constexpr int kKBytes = kChunks * kKChunkBytes;          // 147456
-constexpr int kPAllBytes = 4 * kPBytes;                  // 32768
-// 12 warps = 3 per SM sub-partition, which leaves 168 registers per thread.
 constexpr int kThreads = 384;
 constexpr int kSoftmaxThreads = 128;       // warps 0..3 (TMEM lane quadrants 0..3); lane 0 of warp 0 issues MMAs
-constexpr int kGatherThreads = 256;        // warps 4..11
-constexpr int kGatherWarps = kGatherThreads / 32;
 constexpr int kSoftmaxWarps = kSoftmaxThreads / 32;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 128;            // S_b at kSCol + 32 b, b = 0..4 (4 = rope)
+constexpr uint32_t kSCol = 256;            // S^T
+constexpr uint32_t kLoCol = 320;           // K_lo, 256 dims (128 columns) per pass
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 constexpr float kFp16Max = 65504.0f;
 
 constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kHeads, 0, 0);
-constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 0);
+constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
 
 struct Misc {
-  uint64_t q_ready, meta_ready, s_full, p_ready, pv_done, teardown;
+  uint64_t q_ready, meta_ready, s_full, p_ready, pv_done, teardown, klo_free;
   uint64_t kv_ready[5];                    // latent blocks 0..3 (two chunks each), rope
+  uint64_t klo_ready[2];                   // K_lo of dims 0..255, 256..511 written to TMEM
   uint64_t chunk_free[4];
   uint32_t tmem_slot;
   int abort;
   int need_rescale;
   int stop;
   int range_err;
-  int f_set;
-  int scmax[4];                            // running max of the block scales (float bits, >= 0)
-  float f[4];                              // power-of-two factor carried by P_j
   float red[4][kHeads];
   float m_used[kHeads];
   float alpha[kHeads];
   float lse_out[kHeads];
   float linv[kHeads];
-  float sc[kTile][4];                      // block scales of the tile's tokens
   unsigned char valid[kTile];
 };
 
-constexpr size_t kSmemBytes = 1024 + kQBytes + kKBytes + kPAllBytes + sizeof(Misc);
+constexpr size_t kSmemBytes = 1024 + kQBytes + kKBytes + sizeof(Misc);
 
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {  // byte offset in a 128B-swizzled chunk
   return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
-// 4 E4M3 codes -> 4 fp16 (exact).
-__device__ __forceinline__ uint2 codes4(uint32_t w) {
-  return make_uint2(e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu)), e4m3x2_to_f16x2((uint16_t)(w >> 16)));
+// Two E4M3 codes times a scale, split into fp16 hi and lo parts: k = hi + lo (+ ~2^-22 k).
+__device__ __forceinline__ void dq2(uint16_t two, float sc, uint32_t& hi, uint32_t& lo, int& range_bad) {
+  const float2 c = f16x2_to_f32x2(e4m3x2_to_f16x2(two));
+  const float k0 = c.x * sc, k1 = c.y * sc;
+  range_bad |= !(fabsf(k0) <= kFp16Max) | !(fabsf(k1) <= kFp16Max);
+  hi = f32x2_to_f16x2_sat(k0, k1);
+  const float2 h = f16x2_to_f32x2(hi);
+  lo = f32x2_to_f16x2_sat(k0 - h.x, k1 - h.y);
 }
 
 // 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
@@ -117,30 +110,26 @@ __device__ __forceinline__ uint4 bf8_to_h8(uint4 v, int& range_bad) {
                     bf2_to_h2(v.w, range_bad));
 }
 
-__device__ __forceinline__ uint16_t f32_to_f16_sat(float x) {
-  return (uint16_t)(f32x2_to_f16x2_sat(x, 0.f) & 0xFFFFu);
-}
-
-// Warp reduce-scatter over 32 per-thread values: afterwards lane l holds the
-// reduction over the warp's 32 threads of column l.
+// Warp reduce-scatter over 64 per-thread values: afterwards lane l holds the
+// reduction over the warp's 32 threads of columns 2l and 2l+1.
 template <bool kMax>
-__device__ __forceinline__ float reduce_scatter32(const float (&v)[32], int lane) {
-  float a[16];
+__device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lane) {
+  float a[32];
   {
     const bool hi = lane & 16;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float send = hi ? v[i] : v[16 + i];
-      const float keep = hi ? v[16 + i] : v[i];
+    for (int i = 0; i < 32; ++i) {
+      const float send = hi ? v[i] : v[32 + i];
+      const float keep = hi ? v[32 + i] : v[i];
       const float r = __shfl_xor_sync(0xffffffffu, send, 16);
       a[i] = kMax ? fmaxf(keep, r) : keep + r;
     }
   }
 #pragma unroll
-  for (int span = 8, x = 8; span >= 1; span >>= 1, x >>= 1) {
+  for (int span = 16, x = 8; span >= 2; span >>= 1, x >>= 1) {
     const bool hi = lane & x;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 16; ++i) {
       if (i < span) {
         const float send = hi ? a[i] : a[span + i];
         const float keep = hi ? a[span + i] : a[i];
@@ -149,13 +138,13 @@ __device__ __forceinline__ float reduce_scatter32(const float (&v)[32], int lane
       }
     }
   }
-  return a[0];
+  return make_float2(a[0], a[1]);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Misc& ms = *reinterpret_cast<Misc*>(base + kQBytes + kKBytes + kPAllBytes);
+  Misc& ms = *reinterpret_cast<Misc*>(base + kQBytes + kKBytes);
   volatile int* abort = &ms.abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -166,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const int hg_valid = min(kHeads, p.H - kHeads * g);
   const uint32_t q_base = ptx::smem_u32(base);
   const uint32_t k_base = q_base + kQBytes;
-  const uint32_t p_base = k_base + kKBytes;
+  const uint32_t p_base = k_base + 8 * kKChunkBytes;   // P over the rope chunk
 
   if (n_tiles == 0) {
     // empty partition: out = 0, lse = -inf
@@ -186,22 +175,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   if (threadIdx.x == 0) {
     // producer barriers count one arrival per warp (lane 0 after the warp's fences)
     ptx::mbar_init(&ms.q_ready, kSoftmaxWarps);
-    ptx::mbar_init(&ms.meta_ready, kGatherWarps);
+    ptx::mbar_init(&ms.meta_ready, 4);
     ptx::mbar_init(&ms.s_full, 1);
     ptx::mbar_init(&ms.p_ready, kSoftmaxWarps);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
-    for (int c = 0; c < 5; ++c) ptx::mbar_init(&ms.kv_ready[c], kGatherWarps);
+    ptx::mbar_init(&ms.klo_free, 1);
+    for (int c = 0; c < 4; ++c) ptx::mbar_init(&ms.kv_ready[c], 4);
+    ptx::mbar_init(&ms.kv_ready[4], 8);
+    ptx::mbar_init(&ms.klo_ready[0], 4);
+    ptx::mbar_init(&ms.klo_ready[1], 4);
     for (int j = 0; j < 4; ++j) ptx::mbar_init(&ms.chunk_free[j], 1);
     ms.abort = 0;
     ms.need_rescale = 0;
     ms.stop = 0;
     ms.range_err = 0;
-    ms.f_set = 0;
-    for (int j = 0; j < 4; ++j) {
-      ms.scmax[j] = 0;
-      ms.f[j] = 1.f;
-    }
     ptx::fence_mbar_init();
   }
   if (threadIdx.x < kHeads) {
@@ -219,30 +207,34 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const uint32_t tmem = ms.tmem_slot;
 
   if (warp >= 4) {
-    // ------------------------------------------------------------------ gather + convert
-    const int gid = threadIdx.x - kSoftmaxThreads;
-    const int tl = gid >> 1, half = gid & 1;
+    // ------------------------------------------------------------------ gather + dequantise
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    const int h2 = (warp - 4) >> 2;            // latent dims [256 h2, 256 h2 + 256)
+    const int t = 32 * quad + lane;            // token within the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
     const int seq_len = __ldg(p.seq_lens + b);
     const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
     const int32_t* tk_row = p.topk + (size_t)b * p.topk_n;
     int range_bad = 0;
 
-    uint4 lat[16], rope[4], scv = make_uint4(0, 0, 0, 0);
+    uint4 lat[16], rope[4];
+    float sc0 = 0.f, sc1 = 0.f;                // scales of latent blocks 2 h2, 2 h2 + 1
     auto load_row = [&](int64_t r) {
       if (r >= 0) {
         const unsigned char* rec = p.kv + r * kRecordBytes;
 #pragma unroll
-        for (int k = 0; k < 16; ++k) lat[k] = ptx::ldg_stream(rec + 16 * (2 * k + half));
+        for (int k = 0; k < 16; ++k) lat[k] = __ldg(reinterpret_cast<const uint4*>(rec + 256 * h2) + k);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) rope[k] = ptx::ldg_stream(rec + 528 + 16 * (2 * k + half));
-        scv = ptx::ldg_stream(rec + 512);
+        for (int k = 0; k < 4; ++k) rope[k] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 64 * h2) + k);
+        const float2 sc = __ldg(reinterpret_cast<const float2*>(rec + 512 + 8 * h2));
+        sc0 = sc.x;
+        sc1 = sc.y;
       }
     };
     auto topk_at = [&](int i) -> int {
-      const int pos = pos0 + i * kTile + tl;
+      const int pos = pos0 + i * kTile + t;
       return pos < pos_end ? __ldg(tk_row + pos) : -1;
     };
-
     int64_t row = row_of(bt_row, topk_at(0), seq_len, p.max_pages, p.num_pages, p.err);
     load_row(row);
 
@@ -250,59 +242,64 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     for (int i = 0; ok && i < n_tiles; ++i) {
       const int t_next = (i + 1 < n_tiles) ? topk_at(i + 1) : -1;
       const bool valid = row >= 0;
-      // latent block j = chunks 2j, 2j+1; this thread owns units 4c+half and 4c+2+half of chunk c
+      // latent blocks 2 h2 and 2 h2 + 1 (chunks 4 h2 .. 4 h2 + 3): K_hi into shared memory, K_lo into
+      // TMEM lane t.  The K_lo columns hold dims 0..255 first and 256..511 after the first correction
+      // pass of this tile has read them (klo_free); the previous tile's passes are complete once its
+      // PV has freed a chunk.
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort))) {
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * h2 + jj;
+        bool w_ok = true;
+        if (i > 0) w_ok = ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort);
+        if (jj == 0 && h2 == 1 && w_ok) w_ok = ptx::mbar_wait_bounded(&ms.klo_free, i & 1, abort);
+        if (!__all_sync(0xffffffffu, w_ok)) {
           ok = false;
           break;
         }
-        if (j == 0) {
-          float sv[4] = {valid ? __uint_as_float(scv.x) : 0.f, valid ? __uint_as_float(scv.y) : 0.f,
-                         valid ? __uint_as_float(scv.z) : 0.f, valid ? __uint_as_float(scv.w) : 0.f};
-          if (half == 0) {
-            ms.valid[tl] = valid;
-            ms.sc[tl][0] = sv[0]; ms.sc[tl][1] = sv[1]; ms.sc[tl][2] = sv[2]; ms.sc[tl][3] = sv[3];
-          }
+        ptx::tc_fence_after();
+        if (jj == 0 && h2 == 0) ms.valid[t] = valid;
+        const float sc = jj == 0 ? sc0 : sc1;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float m = fabsf(sv[q]);
-#pragma unroll
-            for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            sv[q] = m;
-          }
-          __syncwarp();
-          if (lane == 0) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (sv[q] > 0.f) atomicMax(&ms.scmax[q], __float_as_int(sv[q]));
-            ptx::mbar_arrive(&ms.meta_ready);
-          }
-        }
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * j + cc;
+        for (int u0 = 0; u0 < 8; u0 += 2) {      // pairs of 16-dim units of this block
+          uint32_t lo[16];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int k = 2 * c + e;                  // lat[] index: unit u = 2k + half
-            const int uc = (2 * k + half) & 3;        // 16-dim unit within the chunk
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-            if (valid) {
-              const uint2 a0 = codes4(lat[k].x), a1 = codes4(lat[k].y), a2 = codes4(lat[k].z), a3 = codes4(lat[k].w);
-              lo = make_uint4(a0.x, a0.y, a1.x, a1.y);
-              hi = make_uint4(a2.x, a2.y, a3.x, a3.y);
+            const int u = u0 + e, k = 8 * jj + u;
+            const uint32_t w[4] = {lat[k].x, lat[k].y, lat[k].z, lat[k].w};
+            uint32_t hv[8];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              dq2((uint16_t)(w[q] & 0xFFFFu), sc, hv[2 * q], lo[8 * e + 2 * q], range_bad);
+              dq2((uint16_t)(w[q] >> 16), sc, hv[2 * q + 1], lo[8 * e + 2 * q + 1], range_bad);
             }
+            if (!valid) {
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                hv[q] = 0u;
+                lo[8 * e + q] = 0u;
+              }
+            }
+            const int c = 2 * j + (u >> 2);         // chunk of this unit
             const uint32_t cb = k_base + c * kKChunkBytes;
-            ptx::sts128(cb + swz(tl, 2 * uc), lo);
-            ptx::sts128(cb + swz(tl, 2 * uc + 1), hi);
+            const int uc = u & 3;
+            ptx::sts128(cb + swz(t, 2 * uc), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+            ptx::sts128(cb + swz(t, 2 * uc + 1), make_uint4(hv[4], hv[5], hv[6], hv[7]));
           }
+          ptx::tmem_st16(tmem + lane_base + kLoCol + 64 * jj + 8 * u0, lo);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[j]);
+        if (lane == 0) {
+          if (jj == 0 && h2 == 0) ptx::mbar_arrive(&ms.meta_ready);
+          ptx::mbar_arrive(&ms.kv_ready[j]);
+        }
       }
       if (!ok) break;
-      // rope chunk: free once the previous tile's PV is done (all of its MMAs have completed)
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[h2]);
+      // rope chunk: free once the previous tile's PV is done (its P lives there)
       if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort))) {
         ok = false;
         break;
@@ -310,10 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       {
         const uint32_t cb = k_base + 8 * kKChunkBytes;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int r = 2 * k + half;
-          ptx::sts128(cb + swz(tl, r), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
-        }
+        for (int k = 0; k < 4; ++k)
+          ptx::sts128(cb + swz(t, 4 * h2 + k), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
@@ -336,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
       const uint16_t* qg = p.q + ((size_t)b * p.H + (size_t)g * kHeads) * kDQK;
 #pragma unroll 1
-      for (int k0 = 0; k0 < 18; k0 += 9) {
+      for (int k0 = 0; k0 < 36; k0 += 9) {
         uint4 v[9];
 #pragma unroll
         for (int k = 0; k < 9; ++k) {
@@ -357,82 +352,83 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     }
     const float c2 = p.sm_scale * 1.4426950408889634f;
     const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-    float lsum = 0.f;                             // this warp's sum for head `lane`
+    float lsum0 = 0.f, lsum1 = 0.f;               // this warp's sums for heads 2*lane, 2*lane+1
     bool ok = true;
     bool mma_ok = true;                           // issuer only
     if (issuer) mma_ok = ptx::mbar_wait_bounded(&ms.q_ready, 0, abort);
     for (int i = 0; i < n_tiles; ++i) {
       const uint32_t ph = i & 1;
       if (issuer && mma_ok) {
-        // QK: latent block j (chunks 2j, 2j+1) into S_j, then the rope chunk into S_4
-        for (int j = 0; mma_ok && j < 5; ++j) {
-          mma_ok = ptx::mbar_wait_bounded(&ms.kv_ready[j], ph, abort);
-          if (!mma_ok) break;
-          ptx::tc_fence_after();
-          const int c0 = j < 4 ? 2 * j : 8, nc = j < 4 ? 2 : 1;
-          for (int cc = 0; cc < nc; ++cc) {
-            const int c = c0 + cc;
+        // QK: K_hi blocks 0, 1 | correction dims 0..255 | K_hi blocks 2, 3 | rope | correction dims 256..511
+        const uint32_t dS = tmem + kSCol;
+        for (int step = 0; mma_ok && step < 7; ++step) {
+          if (step == 2 || step == 6) {
+            const int pass = step == 2 ? 0 : 1;
+            mma_ok = ptx::mbar_wait_bounded(&ms.klo_ready[pass], ph, abort);
+            if (!mma_ok) break;
+            ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t da = ptx::sw128_desc(k_base + c * kKChunkBytes + kk * 32, 16, 1024);
-              const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + kk * 32, 16, 1024);
-              // the first MMA into a block's accumulator overwrites it
-              ptx::mma_f16_ss(tmem + kSCol + 32 * j, da, db, kIdescQK, (cc | kk) != 0);
+            for (int kk = 0; kk < 16; ++kk) {
+              const int c = 4 * pass + (kk >> 2);
+              const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + (kk & 3) * 32, 16, 1024);
+              ptx::mma_f16_ts(dS, tmem + kLoCol + 8 * kk, db, kIdescQK, 1u);
+            }
+            ptx::mma_commit(pass == 0 ? &ms.klo_free : &ms.s_full);
+          } else {
+            const int j = step < 2 ? step : step - 1;   // 0, 1, 2, 3, 4 (rope)
+            mma_ok = ptx::mbar_wait_bounded(&ms.kv_ready[j], ph, abort);
+            if (!mma_ok) break;
+            ptx::tc_fence_after();
+            const int c0 = j < 4 ? 2 * j : 8, nc = j < 4 ? 2 : 1;
+            for (int cc = 0; cc < nc; ++cc) {
+              const int c = c0 + cc;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t da = ptx::sw128_desc(k_base + c * kKChunkBytes + kk * 32, 16, 1024);
+                const uint64_t db = ptx::sw128_desc(q_base + c * kQChunkBytes + kk * 32, 16, 1024);
+                ptx::mma_f16_ss(dS, da, db, kIdescQK, (c | kk) != 0);   // the very first MMA overwrites S
+              }
             }
           }
         }
-        if (mma_ok) ptx::mma_commit(&ms.s_full);
       }
       ok = ptx::mbar_wait_bounded(&ms.meta_ready, ph, abort) && ptx::mbar_wait_bounded(&ms.s_full, ph, abort);
       ok = __all_sync(0xffffffffu, ok);
       ptx::tc_fence_after();
-      const float scb[4] = {ms.sc[t][0], ms.sc[t][1], ms.sc[t][2], ms.sc[t][3]};
-      float s[32];
+      float s[64];
       {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + lane_base + kSCol + 128, r);   // rope accumulator
-        ptx::tmem_wait_ld();
+        const bool valid = ms.valid[t];
 #pragma unroll
-        for (int h = 0; h < 32; ++h) s[h] = __uint_as_float(r[h]);
-#pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          ptx::tmem_ld32(tmem + lane_base + kSCol + 32 * bb, r);
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tmem + lane_base + kSCol + 32 * hh, r);
           ptx::tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) s[h] = fmaf(scb[bb], __uint_as_float(r[h]), s[h]);
+          for (int h = 0; h < 32; ++h) s[32 * hh + h] = valid ? __uint_as_float(r[h]) * c2 : -CUDART_INF_F;
         }
       }
-      const bool valid = ms.valid[t];
-#pragma unroll
-      for (int h = 0; h < 32; ++h) s[h] = valid ? s[h] * c2 : -CUDART_INF_F;
-      const float mx = reduce_scatter32<true>(s, lane);
-      ms.red[warp][lane] = mx;
+      const float2 mx = reduce_scatter64<true>(s, lane);
+      ms.red[warp][2 * lane] = mx.x;
+      ms.red[warp][2 * lane + 1] = mx.y;
       ptx::named_bar_sync(1, kSoftmaxThreads);
       if (warp == 0) {
-        const int h = lane;
-        const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
-        const float mo = ms.m_used[h];
-        float mn = mo, a = 1.f;
         bool resc = false;
-        if (mt > mo + kRescaleThreshold) {        // also true when mo = -inf and mt is finite
-          mn = mt;
-          a = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
-          resc = (mo != -CUDART_INF_F);
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * lane + e;
+          const float mt = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+          const float mo = ms.m_used[h];
+          float mn = mo, a = 1.f;
+          if (mt > mo + kRescaleThreshold) {      // also true when mo = -inf and mt is finite
+            mn = mt;
+            a = (mo == -CUDART_INF_F) ? 0.f : exp2f(mo - mn);
+            resc |= (mo != -CUDART_INF_F);
+          }
+          ms.m_used[h] = mn;
+          ms.alpha[h] = a;
         }
-        ms.m_used[h] = mn;
-        ms.alpha[h] = a;
         const bool any = __any_sync(0xffffffffu, resc);
-        // P_j factor: fixed at the first tile that holds data, so that F_j * max scale is in [0.5, 1)
-        const bool set_now = !ms.f_set && (ms.scmax[0] | ms.scmax[1] | ms.scmax[2] | ms.scmax[3]) != 0;
-        if (set_now && lane < 4) {
-          const float mxs = __int_as_float(ms.scmax[lane]);
-          int e = 0;
-          if (mxs > 0.f) frexpf(mxs, &e);
-          ms.f[lane] = ldexpf(1.f, -e);
-        }
-        __syncwarp();
         if (lane == 0) {
-          if (set_now) ms.f_set = 1;
           ms.need_rescale = any && i > 0;
           ms.stop = *abort || !ok;
         }
@@ -442,36 +438,35 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         ok = false;
         break;
       }
-      // P = exp2(s - m), in place
+      // P row of this token: 64 heads in fp16 (128 B), 128B-swizzled over the rope chunk
 #pragma unroll
-      for (int h = 0; h < 32; ++h) {
-        const float m = ms.m_used[h];
-        s[h] = (m == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m);
-      }
-      // P_j[h][t] = p * scale_j * F_j, K-major (rows = heads, 2 chunks of 64 tokens)
-      {
-        const uint32_t tok_off = (t >> 6) * kPChunkBytes + (t & 7) * 2;
-        const uint32_t unit = (t & 63) >> 3;
+      for (int u = 0; u < 8; ++u) {
+        uint32_t w[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float f = scb[j] * ms.f[j];
-          range_bad |= !(f * 256.f <= kFp16Max);
-          unsigned char* pj = base + kQBytes + kKBytes + j * kPBytes + tok_off;
-#pragma unroll
-          for (int h = 0; h < 32; ++h) *reinterpret_cast<uint16_t*>(pj + swz(h, unit)) = f32_to_f16_sat(s[h] * f);
+        for (int q = 0; q < 4; ++q) {
+          const int h = 8 * u + 2 * q;
+          const float m0 = ms.m_used[h], m1 = ms.m_used[h + 1];
+          s[h] = (m0 == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m0);
+          s[h + 1] = (m1 == -CUDART_INF_F) ? 0.f : exp2f(s[h + 1] - m1);
+          w[q] = f32x2_to_f16x2_sat(s[h], s[h + 1]);
         }
+        ptx::sts128(p_base + swz(t, u), make_uint4(w[0], w[1], w[2], w[3]));
       }
-      const float ps = reduce_scatter32<false>(s, lane);
-      lsum = lsum * ms.alpha[lane] + ps;
+      const float2 ps = reduce_scatter64<false>(s, lane);
+      lsum0 = lsum0 * ms.alpha[2 * lane] + ps.x;
+      lsum1 = lsum1 * ms.alpha[2 * lane + 1] + ps.y;
       if (ms.need_rescale) {
         for (int j = 0; j < 4; ++j) {
-          uint32_t r[32];
-          const uint32_t ta = tmem + lane_base + 32 * j;
-          ptx::tmem_ld32(ta, r);
-          ptx::tmem_wait_ld();
 #pragma unroll
-          for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * ms.alpha[q]);
-          ptx::tmem_st32(ta, r);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t r[32];
+            const uint32_t ta = tmem + lane_base + 64 * j + 32 * hh;
+            ptx::tmem_ld32(ta, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * ms.alpha[32 * hh + q]);
+            ptx::tmem_st32(ta, r);
+          }
         }
         ptx::tmem_wait_st();
       }
@@ -480,7 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&ms.p_ready);
       if (issuer && mma_ok) {
-        // PV: O_j^T += V_j^T . P_j^T for the four 128-dim blocks
+        // PV: O_j^T += V_j^T . P^T for the four 128-dim blocks
         mma_ok = ptx::mbar_wait_bounded(&ms.p_ready, ph, abort);
         if (mma_ok) {
           ptx::tc_fence_after();
@@ -488,9 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
 #pragma unroll
             for (int kk = 0; kk < kTile / 16; ++kk) {
               const uint64_t da = ptx::sw128_desc(k_base + (2 * j) * kKChunkBytes + kk * 2048, kKChunkBytes, 1024);
-              const uint64_t db =
-                  ptx::sw128_desc(p_base + j * kPBytes + (kk >> 2) * kPChunkBytes + (kk & 3) * 32, 16, 1024);
-              ptx::mma_f16_ss(tmem + 32 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+              // P spans one 64-head atom along N, so its leading offset is never stepped; it is set
+              // equal to the stride so that no reading of the two fields leaves the rope chunk.
+              const uint64_t db = ptx::sw128_desc(p_base + kk * 2048, 1024, 1024);
+              ptx::mma_f16_ss(tmem + 64 * j, da, db, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
             }
             ptx::mma_commit(&ms.chunk_free[j]);
           }
@@ -500,35 +496,42 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       __syncwarp();
     }
     if (range_bad) ms.range_err = 1;
-    // epilogue: O / (l F_j), lse
+    // epilogue: O / l, lse
     if (ok) ok = ptx::mbar_wait_bounded(&ms.pv_done, (n_tiles - 1) & 1, abort);
     ok = __all_sync(0xffffffffu, ok);
     ptx::tc_fence_after();
-    ms.red[warp][lane] = lsum;
+    ms.red[warp][2 * lane] = lsum0;
+    ms.red[warp][2 * lane + 1] = lsum1;
     ptx::named_bar_sync(1, kSoftmaxThreads);
     if (warp == 0) {
-      const int h = lane;
-      const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
-      ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
-      ms.lse_out[h] = L > 0.f ? (ms.m_used[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int h = 2 * lane + e;
+        const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+        ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
+        ms.lse_out[h] = L > 0.f ? (ms.m_used[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+      }
     }
     ptx::named_bar_sync(2, kSoftmaxThreads);
     if (ok) {
       for (int j = 0; j < 4; ++j) {
         const int d = 128 * j + t;
-        const float finv = 1.f / ms.f[j];
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem + lane_base + 32 * j, r);
-        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          if (q < hg_valid) {
-            const float o = __uint_as_float(r[q]) * (ms.linv[q] * finv);
-            const size_t h = (size_t)g * kHeads + q;
-            if (p.final_out) {
-              p.out[((size_t)b * p.H + h) * kDLatent + d] = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
-            } else {
-              p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = o;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          ptx::tmem_ld32(tmem + lane_base + 64 * j + 32 * hh, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) {
+            const int hl = 32 * hh + q;
+            if (hl < hg_valid) {
+              const float o = __uint_as_float(r[q]) * ms.linv[hl];
+              const size_t h = (size_t)g * kHeads + hl;
+              if (p.final_out) {
+                p.out[((size_t)b * p.H + h) * kDLatent + d] = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
+              } else {
+                p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = o;
+              }
             }
           }
         }

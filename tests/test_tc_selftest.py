@@ -1,5 +1,5 @@
-"""tcgen05 building blocks (swizzled fill, K-major and MN-major descriptors, per-block
-accumulators, TMEM loads) on one CTA, checked against a float32 matmul of the same fp16 operands."""
+"""tcgen05 building blocks (swizzled fill, K-major and MN-major descriptors, A operand from TMEM,
+TMEM loads and stores) on one CTA, checked against a float32 matmul of the same fp16 operands."""
 import ctypes as C
 import os
 import subprocess
@@ -22,29 +22,26 @@ def _build():
                         "-Xcompiler", "-fPIC", "-cudart", "shared",
                         "-I", os.path.dirname(hdr), src, "-o", out], check=True)
     lib = C.CDLL(out)
-    lib.tc_selftest.argtypes = [C.c_void_p] * 6
+    lib.tc_selftest.argtypes = [C.c_void_p] * 7
     return lib
 
 
-def test_qk_blocks_and_pv_layouts():
+def test_qk_correction_and_pv_layouts():
     lib = _build()
     g = torch.Generator().manual_seed(7)
     A = torch.randn(128, 576, generator=g).half()
-    Q = torch.randn(32, 576, generator=g).half()
-    P = torch.rand(4, 128, 32, generator=g).half()
-    S = torch.full((5, 128, 32), float("nan"), device="cuda")
-    O = torch.full((512, 32), float("nan"), device="cuda")
+    Q = torch.randn(64, 576, generator=g).half()
+    L = (torch.randn(128, 512, generator=g) * 1e-3).half()
+    P = torch.rand(128, 64, generator=g).half()
+    S = torch.full((128, 64), float("nan"), device="cuda")
+    O = torch.full((512, 64), float("nan"), device="cuda")
     st = torch.full((1,), -1, dtype=torch.int32, device="cuda")
-    dA, dQ, dP = A.cuda(), Q.cuda(), P.cuda()
-    rc = lib.tc_selftest(dA.data_ptr(), dQ.data_ptr(), dP.data_ptr(), S.data_ptr(), O.data_ptr(), st.data_ptr())
+    d = [x.cuda() for x in (A, Q, L, P)]
+    rc = lib.tc_selftest(*[x.data_ptr() for x in d], S.data_ptr(), O.data_ptr(), st.data_ptr())
     assert rc == 0 and int(st.item()) == 0
-    S, O = S.cpu(), O.cpu()
-    Af, Qf = A.float(), Q.float()
-    for b in range(4):
-        ref = Af[:, 128 * b:128 * b + 128] @ Qf[:, 128 * b:128 * b + 128].T
-        assert torch.allclose(S[b], ref, rtol=1e-4, atol=1e-3), (b, (S[b] - ref).abs().max())
-    ref = Af[:, 512:] @ Qf[:, 512:].T
-    assert torch.allclose(S[4], ref, rtol=1e-4, atol=1e-3), (S[4] - ref).abs().max()
-    for j in range(4):
-        ref = Af[:, 128 * j:128 * j + 128].T @ P[j].float()
-        assert torch.allclose(O[128 * j:128 * j + 128], ref, rtol=1e-4, atol=1e-3), (j, (O[128 * j:128 * j + 128] - ref).abs().max())
+    S, O = S.cpu().double(), O.cpu().double()
+    Ad, Qd, Ld, Pd = (x.double() for x in (A, Q, L, P))
+    S_ref = Ad @ Qd.T + Ld @ Qd[:, :512].T
+    assert torch.allclose(S, S_ref, rtol=1e-5, atol=1e-4), (S - S_ref).abs().max()
+    O_ref = Ad[:, :512].T @ Pd
+    assert torch.allclose(O, O_ref, rtol=1e-5, atol=1e-4), (O - O_ref).abs().max()
