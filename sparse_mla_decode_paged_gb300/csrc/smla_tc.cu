@@ -92,7 +92,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {  // byte 
 __device__ __forceinline__ void dq2(uint16_t two, float sc, uint32_t& hi, uint32_t& lo, int& range_bad) {
   const float2 c = f16x2_to_f32x2(e4m3x2_to_f16x2(two));
   const float k0 = c.x * sc, k1 = c.y * sc;
-  range_bad |= !(fabsf(k0) <= kFp16Max) | !(fabsf(k1) <= kFp16Max);
+  range_bad |= (fabsf(k0) > kFp16Max) | (fabsf(k1) > kFp16Max);
   hi = f32x2_to_f16x2_sat(k0, k1);
   const float2 h = f16x2_to_f32x2(hi);
   lo = f32x2_to_f16x2_sat(k0 - h.x, k1 - h.y);
@@ -259,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
         ptx::tc_fence_after();
         if (jj == 0 && h2 == 0) ms.valid[t] = valid;
         const float sc = jj == 0 ? sc0 : sc1;
+        int rb = 0;                              // range check of this block (only counted for a used token)
 #pragma unroll
         for (int u0 = 0; u0 < 8; u0 += 2) {      // pairs of 16-dim units of this block
           uint32_t lo[16];
@@ -269,8 +270,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
             uint32_t hv[8];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              dq2((uint16_t)(w[q] & 0xFFFFu), sc, hv[2 * q], lo[8 * e + 2 * q], range_bad);
-              dq2((uint16_t)(w[q] >> 16), sc, hv[2 * q + 1], lo[8 * e + 2 * q + 1], range_bad);
+              dq2((uint16_t)(w[q] & 0xFFFFu), sc, hv[2 * q], lo[8 * e + 2 * q], rb);
+              dq2((uint16_t)(w[q] >> 16), sc, hv[2 * q + 1], lo[8 * e + 2 * q + 1], rb);
             }
             if (!valid) {
 #pragma unroll
@@ -287,6 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           }
           ptx::tmem_st16(tmem + lane_base + kLoCol + 64 * jj + 8 * u0, lo);
         }
+        if (valid) range_bad |= rb;
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -309,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           ptx::sts128(cb + swz(t, 4 * h2 + k), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
+        // (bf8_to_h8 only runs for a used token, so its range check only counts those)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
