@@ -6,12 +6,14 @@
 //   gather warps (8)   index -> row through the block table (a1); 16-byte
 //                      loads of each 656-byte record into registers (warp w
 //                      owns the 32 tokens of TMEM lane quadrant w % 4 and one
-//                      half of the latent dims); dequantisation (a2):
-//                      k = e4m3(code) * scale in fp32, split as
-//                      k = K_hi + K_lo with K_hi = fp16(k) stored 128B-swizzled
-//                      into the K tile (9 chunks of 64 dims) and
-//                      K_lo = fp16(k - K_hi) written into TMEM; bf16 rope to
-//                      fp16 (exact).  The next tile's loads follow at once.
+//                      half of the latent dims); dequantisation (a2): the
+//                      block scale is cut into s1 (its leading 7 significant
+//                      bits) and s2 = scale - s1, so K_hi = code * s1 is exact
+//                      in fp16 (4 + 7 bits) and K_lo = code * s2 carries the
+//                      rest (two packed fp16 multiplies per two codes); K_hi is
+//                      stored 128B-swizzled into the K tile (9 chunks of 64
+//                      dims) and K_lo written into TMEM; bf16 rope to fp16
+//                      (exact).  The next tile's loads follow at once.
 //   MMA (warp 0 lane 0) S^T[128 tok x 64 heads] = K_hi . Q^T from shared
 //                      memory (36 MMAs M=128 N=64 K=16) plus the correction
 //                      K_lo . Q^T with the A operand read from TMEM (two
@@ -60,6 +62,7 @@ constexpr uint32_t kSCol = 256;            // S^T
 constexpr uint32_t kLoCol = 320;           // K_lo, 256 dims (128 columns) per pass
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P stays <= 256
 constexpr float kFp16Max = 65504.0f;
+constexpr float kMaxScale = kFp16Max / 448.0f;   // largest block scale whose dequantised latent fits fp16
 
 constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kHeads, 0, 0);
 constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
@@ -75,8 +78,8 @@ struct Misc {
   int stop;
   int range_err;
   float red[4][kHeads];
-  float m_used[kHeads];
-  float alpha[kHeads];
+  alignas(16) float m_used[kHeads];
+  alignas(16) float alpha[kHeads];
   float lse_out[kHeads];
   float linv[kHeads];
   unsigned char valid[kTile];
@@ -88,14 +91,41 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {  // byte 
   return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
-// Two E4M3 codes times a scale, split into fp16 hi and lo parts: k = hi + lo (+ ~2^-22 k).
-__device__ __forceinline__ void dq2(uint16_t two, float sc, uint32_t& hi, uint32_t& lo, int& range_bad) {
-  const float2 c = f16x2_to_f32x2(e4m3x2_to_f16x2(two));
-  const float k0 = c.x * sc, k1 = c.y * sc;
-  range_bad |= (fabsf(k0) > kFp16Max) | (fabsf(k1) > kFp16Max);
-  hi = f32x2_to_f16x2_sat(k0, k1);
-  const float2 h = f16x2_to_f32x2(hi);
-  lo = f32x2_to_f16x2_sat(k0 - h.x, k1 - h.y);
+// The fp16 pair factors (s1, s1) and (s2, s2) of a block scale: s1 keeps the
+// leading 7 significant bits of the fp32 scale, s2 = scale - s1 (exact in fp32,
+// then rounded to fp16).  An E4M3 value has at most 4 significant bits, so
+// code * s1 fits fp16's 11 exactly; |code * s2| < 2^-6 |code * scale|.
+struct ScalePair {
+  uint32_t s1, s2;
+};
+
+__device__ __forceinline__ ScalePair split_scale(float sc) {
+  const float s1 = __uint_as_float(__float_as_uint(sc) & 0xFFFE0000u);
+  const float s2 = sc - s1;
+  const uint32_t a = f32x2_to_f16x2_sat(s1, s1), c = f32x2_to_f16x2_sat(s2, s2);
+  return {a, c};
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// (s2 / s1) as an fp16 pair: K_lo = K_hi * (s2 / s1) for the same codes.
+__device__ __forceinline__ uint32_t hmul2_ratio(const ScalePair& sp) {
+  const float2 a = f16x2_to_f32x2(sp.s1), c = f16x2_to_f32x2(sp.s2);
+  const float r = a.x != 0.f ? c.x / a.x : 0.f;
+  return f32x2_to_f16x2_sat(r, r);
+}
+
+// Four E4M3 codes (one 32-bit word) -> K_hi (exact) and K_lo, two f16x2 words each.
+__device__ __forceinline__ void split4(uint32_t w, const ScalePair& sp, uint32_t (&hi)[2], uint32_t (&lo)[2]) {
+  const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu)), c1 = e4m3x2_to_f16x2((uint16_t)(w >> 16));
+  hi[0] = hmul2(c0, sp.s1);
+  hi[1] = hmul2(c1, sp.s1);
+  lo[0] = hmul2(c0, sp.s2);
+  lo[1] = hmul2(c1, sp.s2);
 }
 
 // 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
@@ -139,6 +169,155 @@ __device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lan
     }
   }
   return make_float2(a[0], a[1]);
+}
+
+// Gather role of warps 4..11: H2 selects the half of the latent dims (and rope) the warp owns.
+template <int H2>
+__device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, volatile int* abort, uint32_t tmem,
+                                            uint32_t k_base, int warp, int lane, int b, int pos0, int pos_end,
+                                            int n_tiles) {
+    // ------------------------------------------------------------------ gather + dequantise
+    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
+    constexpr int h2 = H2;                     // latent dims [256 h2, 256 h2 + 256)
+    const int t = 32 * quad + lane;            // token within the tile = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const int seq_len = __ldg(p.seq_lens + b);
+    const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
+    const int32_t* tk_row = p.topk + (size_t)b * p.topk_n;
+    int range_bad = 0;
+
+    uint4 lat[16], rope[4];
+    float sc0 = 0.f, sc1 = 0.f;                // scales of latent blocks 2 h2, 2 h2 + 1
+    auto load_row = [&](int64_t r) {
+      if (r >= 0) {
+        const unsigned char* rec = p.kv + r * kRecordBytes;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) lat[k] = __ldg(reinterpret_cast<const uint4*>(rec + 256 * h2) + k);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) rope[k] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 64 * h2) + k);
+        const float2 sc = __ldg(reinterpret_cast<const float2*>(rec + 512 + 8 * h2));
+        sc0 = sc.x;
+        sc1 = sc.y;
+      }
+    };
+    auto topk_at = [&](int i) -> int {
+      const int pos = pos0 + i * kTile + t;
+      return pos < pos_end ? __ldg(tk_row + pos) : -1;
+    };
+    int64_t row = row_of(bt_row, topk_at(0), seq_len, p.max_pages, p.num_pages, p.err);
+    load_row(row);
+
+    bool ok = true;
+    for (int i = 0; ok && i < n_tiles; ++i) {
+      const int t_next = (i + 1 < n_tiles) ? topk_at(i + 1) : -1;
+      const bool valid = row >= 0;
+      // latent blocks 2 h2 and 2 h2 + 1 (chunks 4 h2 .. 4 h2 + 3): K_hi into shared memory and, for the
+      // first half of the dims, K_lo into TMEM lane t at once.  The K_lo columns take dims 256..511 only
+      // after the first correction pass of this tile has read them (klo_free), so the second-half warps
+      // write their K_lo in a second, cheap pass.  The previous tile's passes are complete once its PV
+      // has freed a chunk.
+      const ScalePair spb[2] = {split_scale(sc0), split_scale(sc1)};
+      if (valid) range_bad |= !(fabsf(sc0) <= kMaxScale) | !(fabsf(sc1) <= kMaxScale);
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * h2 + jj;
+        if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort))) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (jj == 0 && h2 == 0) ms.valid[t] = valid;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {            // 16-dim units of this block
+          const int k = 8 * jj + u;
+          const uint32_t w[4] = {lat[k].x, lat[k].y, lat[k].z, lat[k].w};
+          uint32_t hv[8], lo[8];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t h[2], l[2];
+            split4(w[q], spb[jj], h, l);
+            hv[2 * q] = valid ? h[0] : 0u;
+            hv[2 * q + 1] = valid ? h[1] : 0u;
+            lo[2 * q] = valid ? l[0] : 0u;
+            lo[2 * q + 1] = valid ? l[1] : 0u;
+          }
+          const int c = 2 * j + (u >> 2);         // chunk of this unit
+          const uint32_t cb = k_base + c * kKChunkBytes;
+          const int uc = u & 3;
+          ptx::sts128(cb + swz(t, 2 * uc), make_uint4(hv[0], hv[1], hv[2], hv[3]));
+          ptx::sts128(cb + swz(t, 2 * uc + 1), make_uint4(hv[4], hv[5], hv[6], hv[7]));
+          if (h2 == 0) ptx::tmem_st8(tmem + lane_base + kLoCol + 64 * jj + 8 * u, lo);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          if (jj == 0 && h2 == 0) ptx::mbar_arrive(&ms.meta_ready);
+          ptx::mbar_arrive(&ms.kv_ready[j]);
+        }
+      }
+      if (!ok) break;
+      if (h2 == 0) {
+        // K_lo of dims 0..255 is in TMEM already
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[0]);
+      }
+      // rope chunk: free once the previous tile's PV is done (its P lives there)
+      if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort))) {
+        ok = false;
+        break;
+      }
+      {
+        const uint32_t cb = k_base + 8 * kKChunkBytes;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          ptx::sts128(cb + swz(t, 4 * h2 + k), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
+        // (bf8_to_h8 only runs for a used token, so its range check only counts those)
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
+      }
+      // the codes of this tile are consumed: start the next tile's loads
+      const uint32_t r_lo[2] = {hmul2_ratio(spb[0]), hmul2_ratio(spb[1])};
+      if (i + 1 < n_tiles) {
+        row = row_of(bt_row, t_next, seq_len, p.max_pages, p.num_pages, p.err);
+        load_row(row);
+      }
+      if (h2 == 1) {
+        // K_lo of dims 256..511 = K_hi * (s2 / s1), from this thread's own K_hi rows, once the first
+        // correction pass of this tile has read the TMEM columns
+        if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.klo_free, i & 1, abort))) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+#pragma unroll
+          for (int u0 = 0; u0 < 8; u0 += 2) {
+            uint32_t lo[16];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int u = u0 + e;
+              const int c = 2 * (2 * h2 + jj) + (u >> 2);
+              const uint32_t cb = k_base + c * kKChunkBytes;
+              const uint4 h0 = ptx::lds128(cb + swz(t, 2 * (u & 3)));
+              const uint4 h1 = ptx::lds128(cb + swz(t, 2 * (u & 3) + 1));
+              const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+#pragma unroll
+              for (int q = 0; q < 8; ++q) lo[8 * e + q] = hmul2(hv[q], r_lo[jj]);
+            }
+            ptx::tmem_st16(tmem + lane_base + kLoCol + 64 * jj + 8 * u0, lo);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[1]);
+      }
+    }
+    if (range_bad) ms.range_err = 1;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams p) {
@@ -207,121 +386,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
   const uint32_t tmem = ms.tmem_slot;
 
   if (warp >= 4) {
-    // ------------------------------------------------------------------ gather + dequantise
-    const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
-    const int h2 = (warp - 4) >> 2;            // latent dims [256 h2, 256 h2 + 256)
-    const int t = 32 * quad + lane;            // token within the tile = TMEM lane
-    const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
-    const int seq_len = __ldg(p.seq_lens + b);
-    const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
-    const int32_t* tk_row = p.topk + (size_t)b * p.topk_n;
-    int range_bad = 0;
-
-    uint4 lat[16], rope[4];
-    float sc0 = 0.f, sc1 = 0.f;                // scales of latent blocks 2 h2, 2 h2 + 1
-    auto load_row = [&](int64_t r) {
-      if (r >= 0) {
-        const unsigned char* rec = p.kv + r * kRecordBytes;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) lat[k] = __ldg(reinterpret_cast<const uint4*>(rec + 256 * h2) + k);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) rope[k] = __ldg(reinterpret_cast<const uint4*>(rec + 528 + 64 * h2) + k);
-        const float2 sc = __ldg(reinterpret_cast<const float2*>(rec + 512 + 8 * h2));
-        sc0 = sc.x;
-        sc1 = sc.y;
-      }
-    };
-    auto topk_at = [&](int i) -> int {
-      const int pos = pos0 + i * kTile + t;
-      return pos < pos_end ? __ldg(tk_row + pos) : -1;
-    };
-    int64_t row = row_of(bt_row, topk_at(0), seq_len, p.max_pages, p.num_pages, p.err);
-    load_row(row);
-
-    bool ok = true;
-    for (int i = 0; ok && i < n_tiles; ++i) {
-      const int t_next = (i + 1 < n_tiles) ? topk_at(i + 1) : -1;
-      const bool valid = row >= 0;
-      // latent blocks 2 h2 and 2 h2 + 1 (chunks 4 h2 .. 4 h2 + 3): K_hi into shared memory, K_lo into
-      // TMEM lane t.  The K_lo columns hold dims 0..255 first and 256..511 after the first correction
-      // pass of this tile has read them (klo_free); the previous tile's passes are complete once its
-      // PV has freed a chunk.
-#pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        const int j = 2 * h2 + jj;
-        bool w_ok = true;
-        if (i > 0) w_ok = ptx::mbar_wait_bounded(&ms.chunk_free[j], (i - 1) & 1, abort);
-        if (jj == 0 && h2 == 1 && w_ok) w_ok = ptx::mbar_wait_bounded(&ms.klo_free, i & 1, abort);
-        if (!__all_sync(0xffffffffu, w_ok)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        if (jj == 0 && h2 == 0) ms.valid[t] = valid;
-        const float sc = jj == 0 ? sc0 : sc1;
-        int rb = 0;                              // range check of this block (only counted for a used token)
-#pragma unroll
-        for (int u0 = 0; u0 < 8; u0 += 2) {      // pairs of 16-dim units of this block
-          uint32_t lo[16];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int u = u0 + e, k = 8 * jj + u;
-            const uint32_t w[4] = {lat[k].x, lat[k].y, lat[k].z, lat[k].w};
-            uint32_t hv[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              dq2((uint16_t)(w[q] & 0xFFFFu), sc, hv[2 * q], lo[8 * e + 2 * q], rb);
-              dq2((uint16_t)(w[q] >> 16), sc, hv[2 * q + 1], lo[8 * e + 2 * q + 1], rb);
-            }
-            if (!valid) {
-#pragma unroll
-              for (int q = 0; q < 8; ++q) {
-                hv[q] = 0u;
-                lo[8 * e + q] = 0u;
-              }
-            }
-            const int c = 2 * j + (u >> 2);         // chunk of this unit
-            const uint32_t cb = k_base + c * kKChunkBytes;
-            const int uc = u & 3;
-            ptx::sts128(cb + swz(t, 2 * uc), make_uint4(hv[0], hv[1], hv[2], hv[3]));
-            ptx::sts128(cb + swz(t, 2 * uc + 1), make_uint4(hv[4], hv[5], hv[6], hv[7]));
-          }
-          ptx::tmem_st16(tmem + lane_base + kLoCol + 64 * jj + 8 * u0, lo);
-        }
-        if (valid) range_bad |= rb;
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (jj == 0 && h2 == 0) ptx::mbar_arrive(&ms.meta_ready);
-          ptx::mbar_arrive(&ms.kv_ready[j]);
-        }
-      }
-      if (!ok) break;
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[h2]);
-      // rope chunk: free once the previous tile's PV is done (its P lives there)
-      if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort))) {
-        ok = false;
-        break;
-      }
-      {
-        const uint32_t cb = k_base + 8 * kKChunkBytes;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          ptx::sts128(cb + swz(t, 4 * h2 + k), valid ? bf8_to_h8(rope[k], range_bad) : make_uint4(0, 0, 0, 0));
-        // (bf8_to_h8 only runs for a used token, so its range check only counts those)
-        ptx::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
-      }
-      if (i + 1 < n_tiles) {
-        row = row_of(bt_row, t_next, seq_len, p.max_pages, p.num_pages, p.err);
-        load_row(row);
-      }
-    }
-    if (range_bad) ms.range_err = 1;
+    if (warp < 8) gather_role<0>(p, ms, abort, tmem, k_base, warp, lane, b, pos0, pos_end, n_tiles);
+    else gather_role<1>(p, ms, abort, tmem, k_base, warp, lane, b, pos0, pos_end, n_tiles);
   } else {
     // ------------------------------------------------------------------ Q, MMA issue, softmax, epilogue
     // Every softmax warp runs the same sequence of named barriers; a failed wait
@@ -444,13 +510,16 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       // P row of this token: 64 heads in fp16 (128 B), 128B-swizzled over the rope chunk
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
+        const float4 ma = reinterpret_cast<const float4*>(ms.m_used)[2 * u];
+        const float4 mb = reinterpret_cast<const float4*>(ms.m_used)[2 * u + 1];
+        const float m[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
         uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const int h = 8 * u + 2 * q;
-          const float m0 = ms.m_used[h], m1 = ms.m_used[h + 1];
-          s[h] = (m0 == -CUDART_INF_F) ? 0.f : exp2f(s[h] - m0);
-          s[h + 1] = (m1 == -CUDART_INF_F) ? 0.f : exp2f(s[h + 1] - m1);
+          // a head with no valid entry yet has m = -inf: its P is 0 (s is -inf there too)
+          s[h] = (m[2 * q] == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(s[h] - m[2 * q]);
+          s[h + 1] = (m[2 * q + 1] == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(s[h + 1] - m[2 * q + 1]);
           w[q] = f32x2_to_f16x2_sat(s[h], s[h + 1]);
         }
         ptx::sts128(p_base + swz(t, u), make_uint4(w[0], w[1], w[2], w[3]));
@@ -517,8 +586,11 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
     }
     ptx::named_bar_sync(2, kSoftmaxThreads);
     if (ok) {
+      // O / l staged as rows [head][512] (bf16 or fp32) over the K tile, which every MMA has finished
+      // reading, then one bulk copy per head row
+      const uint32_t elem = p.final_out ? 2u : 4u, row_bytes = 512u * elem;
       for (int j = 0; j < 4; ++j) {
-        const int d = 128 * j + t;
+        const uint32_t d = 128u * j + t;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t r[32];
@@ -526,23 +598,29 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           ptx::tmem_wait_ld();
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
-            const int hl = 32 * hh + q;
-            if (hl < hg_valid) {
-              const float o = __uint_as_float(r[q]) * ms.linv[hl];
-              const size_t h = (size_t)g * kHeads + hl;
-              if (p.final_out) {
-                p.out[((size_t)b * p.H + h) * kDLatent + d] = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
-              } else {
-                p.o_part[(((size_t)b * p.nsplit + split) * p.H + h) * kDLatent + d] = o;
-              }
+            const uint32_t hl = 32 * hh + q;
+            const float o = __uint_as_float(r[q]) * ms.linv[hl];
+            const uint32_t sa = k_base + hl * row_bytes + d * elem;
+            if (p.final_out) {
+              const uint16_t v = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
+              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa), "h"(v) : "memory");
+            } else {
+              asm volatile("st.shared.f32 [%0], %1;" ::"r"(sa), "f"(o) : "memory");
             }
           }
         }
       }
+      ptx::fence_proxy_async_smem();
+      ptx::named_bar_sync(1, kSoftmaxThreads);
       if (t < hg_valid) {
         const size_t h = (size_t)g * kHeads + t;
+        void* dst = p.final_out ? static_cast<void*>(p.out + ((size_t)b * p.H + h) * kDLatent)
+                                : static_cast<void*>(p.o_part + (((size_t)b * p.nsplit + split) * p.H + h) * kDLatent);
+        ptx::bulk_store(dst, k_base + t * row_bytes, row_bytes);
+        ptx::bulk_commit();
         if (p.final_out) p.lse[(size_t)b * p.H + h] = ms.lse_out[t];
         else p.lse_part[((size_t)b * p.nsplit + split) * p.H + h] = ms.lse_out[t];
+        ptx::bulk_wait_read();
       }
     }
     if (issuer) {
