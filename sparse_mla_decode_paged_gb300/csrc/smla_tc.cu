@@ -6,14 +6,15 @@
 //   gather warps (8)   index -> row through the block table (a1); 16-byte
 //                      loads of each 656-byte record into registers (warp w
 //                      owns the 32 tokens of TMEM lane quadrant w % 4 and one
-//                      half of the latent dims); dequantisation (a2): the
-//                      block scale is cut into s1 (its leading 7 significant
-//                      bits) and s2 = scale - s1, so K_hi = code * s1 is exact
-//                      in fp16 (4 + 7 bits) and K_lo = code * s2 carries the
-//                      rest (two packed fp16 multiplies per two codes); K_hi is
+//                      half of the latent dims); dequantisation (a2):
+//                      k = code * scale is split as K_hi = fp16(k) and
+//                      K_lo = k - K_hi with packed fp16 error-free
+//                      multiply-adds (scale = sc_h + s_r, both fp16); K_hi is
 //                      stored 128B-swizzled into the K tile (9 chunks of 64
-//                      dims) and K_lo written into TMEM; bf16 rope to fp16
-//                      (exact).  The next tile's loads follow at once.
+//                      dims), K_lo is written into TMEM in a second pass from
+//                      the thread's own K_hi rows (codes recovered as
+//                      e4m3(K_hi / scale)); bf16 rope to fp16 (exact).  The
+//                      next tile's loads are issued between the two passes.
 //   MMA (warp 0 lane 0) S^T[128 tok x 64 heads] = K_hi . Q^T from shared
 //                      memory (36 MMAs M=128 N=64 K=16) plus the correction
 //                      K_lo . Q^T with the A operand read from TMEM (two
@@ -91,19 +92,17 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) {  // byte 
   return row * 128u + ((unit ^ (row & 7u)) << 4);
 }
 
-// The fp16 pair factors (s1, s1) and (s2, s2) of a block scale: s1 keeps the
-// leading 7 significant bits of the fp32 scale, s2 = scale - s1 (exact in fp32,
-// then rounded to fp16).  An E4M3 value has at most 4 significant bits, so
-// code * s1 fits fp16's 11 exactly; |code * s2| < 2^-6 |code * scale|.
-struct ScalePair {
-  uint32_t s1, s2;
+// fp16 pair factors of a block scale: sc_h = fp16(sc) and s_r = fp16(sc - sc_h), plus 1/sc in fp32.
+struct ScaleSplit {
+  uint32_t sch, sr;
+  float inv;
 };
 
-__device__ __forceinline__ ScalePair split_scale(float sc) {
-  const float s1 = __uint_as_float(__float_as_uint(sc) & 0xFFFE0000u);
-  const float s2 = sc - s1;
-  const uint32_t a = f32x2_to_f16x2_sat(s1, s1), c = f32x2_to_f16x2_sat(s2, s2);
-  return {a, c};
+__device__ __forceinline__ ScaleSplit split_scale(float sc) {
+  const uint32_t h = f32x2_to_f16x2_sat(sc, sc);
+  const float hf = f16x2_to_f32x2(h).x;
+  const float r = sc - hf;                                   // exact in fp32
+  return {h, f32x2_to_f16x2_sat(r, r), sc != 0.f ? 1.f / sc : 0.f};
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -112,20 +111,35 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   return r;
 }
 
-// (s2 / s1) as an fp16 pair: K_lo = K_hi * (s2 / s1) for the same codes.
-__device__ __forceinline__ uint32_t hmul2_ratio(const ScalePair& sp) {
-  const float2 a = f16x2_to_f32x2(sp.s1), c = f16x2_to_f32x2(sp.s2);
-  const float r = a.x != 0.f ? c.x / a.x : 0.f;
-  return f32x2_to_f16x2_sat(r, r);
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
 }
 
-// Four E4M3 codes (one 32-bit word) -> K_hi (exact) and K_lo, two f16x2 words each.
-__device__ __forceinline__ void split4(uint32_t w, const ScalePair& sp, uint32_t (&hi)[2], uint32_t (&lo)[2]) {
-  const uint32_t c0 = e4m3x2_to_f16x2((uint16_t)(w & 0xFFFFu)), c1 = e4m3x2_to_f16x2((uint16_t)(w >> 16));
-  hi[0] = hmul2(c0, sp.s1);
-  hi[1] = hmul2(c1, sp.s1);
-  lo[0] = hmul2(c0, sp.s2);
-  lo[1] = hmul2(c1, sp.s2);
+__device__ __forceinline__ uint32_t hadd2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Two codes c (as fp16, exact) times the scale: K_hi = fp16(c * sc) up to ~2^-22 relative.
+__device__ __forceinline__ uint32_t k_hi2(uint32_t c, const ScaleSplit& sp) {
+  return hfma2(c, sp.sch, hmul2(c, sp.sr));
+}
+
+// K_lo = c * sc - K_hi: fma(c, sc_h, -hi) is exact (the rounding error of a product fits the format),
+// plus the small term c * s_r.
+__device__ __forceinline__ uint32_t k_lo2(uint32_t c, uint32_t hi, const ScaleSplit& sp) {
+  return hadd2(hfma2(c, sp.sch, hi ^ 0x80008000u), hmul2(c, sp.sr));
+}
+
+// The two E4M3 codes behind a K_hi pair: hi / sc is within 2^-10 of a code, far inside half an E4M3 step.
+__device__ __forceinline__ uint32_t codes_of_hi(uint32_t hi, const ScaleSplit& sp) {
+  const float2 f = f16x2_to_f32x2(hi);
+  uint16_t e;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(e) : "f"(f.y * sp.inv), "f"(f.x * sp.inv));
+  return e4m3x2_to_f16x2(e);
 }
 
 // 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
@@ -216,7 +230,7 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
       // after the first correction pass of this tile has read them (klo_free), so the second-half warps
       // write their K_lo in a second, cheap pass.  The previous tile's passes are complete once its PV
       // has freed a chunk.
-      const ScalePair spb[2] = {split_scale(sc0), split_scale(sc1)};
+      const ScaleSplit spb[2] = {split_scale(sc0), split_scale(sc1)};
       if (valid) range_bad |= !(fabsf(sc0) <= kMaxScale) | !(fabsf(sc1) <= kMaxScale);
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
@@ -225,28 +239,22 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
           ok = false;
           break;
         }
-        ptx::tc_fence_after();
         if (jj == 0 && h2 == 0) ms.valid[t] = valid;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {            // 16-dim units of this block
           const int k = 8 * jj + u;
           const uint32_t w[4] = {lat[k].x, lat[k].y, lat[k].z, lat[k].w};
-          uint32_t hv[8], lo[8];
+          uint32_t hv[8];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t h[2], l[2];
-            split4(w[q], spb[jj], h, l);
-            hv[2 * q] = valid ? h[0] : 0u;
-            hv[2 * q + 1] = valid ? h[1] : 0u;
-            lo[2 * q] = valid ? l[0] : 0u;
-            lo[2 * q + 1] = valid ? l[1] : 0u;
+            hv[2 * q] = valid ? k_hi2(e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu)), spb[jj]) : 0u;
+            hv[2 * q + 1] = valid ? k_hi2(e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)), spb[jj]) : 0u;
           }
           const int c = 2 * j + (u >> 2);         // chunk of this unit
           const uint32_t cb = k_base + c * kKChunkBytes;
           const int uc = u & 3;
           ptx::sts128(cb + swz(t, 2 * uc), make_uint4(hv[0], hv[1], hv[2], hv[3]));
           ptx::sts128(cb + swz(t, 2 * uc + 1), make_uint4(hv[4], hv[5], hv[6], hv[7]));
-          if (h2 == 0) ptx::tmem_st8(tmem + lane_base + kLoCol + 64 * jj + 8 * u, lo);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -256,13 +264,6 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
         }
       }
       if (!ok) break;
-      if (h2 == 0) {
-        // K_lo of dims 0..255 is in TMEM already
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[0]);
-      }
       // rope chunk: free once the previous tile's PV is done (its P lives there)
       if (i > 0 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.pv_done, (i - 1) & 1, abort))) {
         ok = false;
@@ -279,43 +280,37 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
         if (lane == 0) ptx::mbar_arrive(&ms.kv_ready[4]);
       }
       // the codes of this tile are consumed: start the next tile's loads
-      const uint32_t r_lo[2] = {hmul2_ratio(spb[0]), hmul2_ratio(spb[1])};
       if (i + 1 < n_tiles) {
         row = row_of(bt_row, t_next, seq_len, p.max_pages, p.num_pages, p.err);
         load_row(row);
       }
-      if (h2 == 1) {
-        // K_lo of dims 256..511 = K_hi * (s2 / s1), from this thread's own K_hi rows, once the first
-        // correction pass of this tile has read the TMEM columns
-        if (!__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.klo_free, i & 1, abort))) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int jj = 0; jj < 2; ++jj) {
-#pragma unroll
-          for (int u0 = 0; u0 < 8; u0 += 2) {
-            uint32_t lo[16];
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int u = u0 + e;
-              const int c = 2 * (2 * h2 + jj) + (u >> 2);
-              const uint32_t cb = k_base + c * kKChunkBytes;
-              const uint4 h0 = ptx::lds128(cb + swz(t, 2 * (u & 3)));
-              const uint4 h1 = ptx::lds128(cb + swz(t, 2 * (u & 3) + 1));
-              const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
-#pragma unroll
-              for (int q = 0; q < 8; ++q) lo[8 * e + q] = hmul2(hv[q], r_lo[jj]);
-            }
-            ptx::tmem_st16(tmem + lane_base + kLoCol + 64 * jj + 8 * u0, lo);
-          }
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[1]);
+      // K_lo into TMEM lane t from this thread's own K_hi rows: dims 0..255 at once (the previous
+      // tile's correction passes are complete once its PV has freed a chunk), dims 256..511 once the
+      // first correction pass of this tile has read the columns (klo_free)
+      if (h2 == 1 && !__all_sync(0xffffffffu, ptx::mbar_wait_bounded(&ms.klo_free, i & 1, abort))) {
+        ok = false;
+        break;
       }
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int c = 2 * (2 * h2 + jj) + (u >> 2);
+          const uint32_t cb = k_base + c * kKChunkBytes;
+          const uint4 h0 = ptx::lds128(cb + swz(t, 2 * (u & 3)));
+          const uint4 h1 = ptx::lds128(cb + swz(t, 2 * (u & 3) + 1));
+          const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+          uint32_t lo[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) lo[q] = k_lo2(codes_of_hi(hv[q], spb[jj]), hv[q], spb[jj]);
+          ptx::tmem_st8(tmem + lane_base + kLoCol + 64 * jj + 8 * u, lo);
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&ms.klo_ready[h2]);
     }
     if (range_bad) ms.range_err = 1;
 }
