@@ -359,7 +359,12 @@ def main_ours(args):
     peak, peak_kind = measured_peaks()
     name = args.workload
     b = Bench(name, dev, seed_offset=rank)
-    steps = args.steps if args.steps else max(b.R, int(1.0 / 5e-6))
+    if args.steps:
+        steps = args.steps
+    else:
+        # about one second of timed calls (enough for clock samples), at least one rotation cycle
+        probe = b.timed(b.call, b.R, 3, world)
+        steps = int(min(200000, max(b.R, 1.0 / max(probe / b.R, 1e-7))))
     visible = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
     gpu_index = visible[local] if local < len(visible) else str(local)
     with ClockSampler(gpu_index) as clk:

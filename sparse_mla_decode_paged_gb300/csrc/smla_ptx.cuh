@@ -140,8 +140,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
       "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      SMLA_W8(0), SMLA_W8(8), SMLA_W8(16), SMLA_W8(24)
-      : "memory");
+      SMLA_W8(0), SMLA_W8(8), SMLA_W8(16), SMLA_W8(24));
 }
 
 // 32 lanes x 16 consecutive 32-bit columns (store).
@@ -149,14 +148,12 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
           taddr),
-      SMLA_W8(0), SMLA_W8(8)
-      : "memory");
+      SMLA_W8(0), SMLA_W8(8));
 }
 
 // 32 lanes x 8 consecutive 32-bit columns (store).
 __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), SMLA_W8(0)
-               : "memory");
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), SMLA_W8(0));
 }
 
 #undef SMLA_R8
@@ -215,6 +212,12 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
   uint4 v;
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(saddr));
   return v;
+}
+
+// Shared store without a compiler memory barrier: for data that only the async proxy (MMA, bulk
+// copy) reads after a proxy fence and a thread barrier, so no C++ access needs ordering against it.
+__device__ __forceinline__ void sts128_async_only(uint32_t saddr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
 }
 
 __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {

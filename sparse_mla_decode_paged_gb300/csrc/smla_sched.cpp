@@ -20,11 +20,11 @@ namespace smla {
 // for one 64-head group, the per-CTA cost of writing fp32 partials, and the
 // merge kernel.
 struct CostModel {
-  double cta_fixed_us = 2.2;
-  double per_token_us = 0.0095;      // per top-k entry for one CTA's head group
-  double partial_write_us = 0.25;    // one head group x 512 fp32 per CTA
-  double combine_fixed_us = 1.6;
-  double combine_gbs = 4000.0;       // partial bytes read + out written
+  double cta_fixed_us = 8.0;         // launch, index chain, Q load, first loads, epilogue
+  double per_tile_us = 16.0;         // one tile of 128 top-k entries for a 64-head group
+  double per_token_us = 0.03;        // partial tiles cost less
+  double combine_fixed_us = 2.0;
+  double combine_gbs = 3000.0;       // partial bytes read + out written
 };
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -57,17 +57,16 @@ static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit
                           int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
   const int hpc = split_heads_per_cta();
   const int head_groups = (H + hpc - 1) / hpc;
-  const int heads_per_cta = H < hpc ? H : hpc;
   const int ctas = B * head_groups * nsplit;
   const double slots = (double)sm_count * ctas_per_sm;
   const double waves = ctas / slots;
   const int whole_waves = (int)ceil(waves - 1e-9);
   const int tokens = split_len < topk ? split_len : topk;
-  const double head_frac = (double)heads_per_cta / hpc;
-  double cta_us = m.cta_fixed_us + m.per_token_us * tokens * (0.5 + 0.5 * head_frac);
+  const int tiles = (tokens + 127) / 128;
+  const double cta_us = m.cta_fixed_us + m.per_tile_us * (tiles - 1) + m.per_token_us * (tokens - 128 * (tiles - 1)) +
+                        (m.per_tile_us - 128 * m.per_token_us);
   double t = whole_waves * cta_us;
   if (nsplit > 1) {
-    t += whole_waves * m.partial_write_us * head_frac;
     const double bytes = (double)B * H * (nsplit * (kDLatent * 4.0 + 4.0) + kDLatent * 2.0 + 4.0);
     t += m.combine_fixed_us + bytes / (m.combine_gbs * 1e3);
   }

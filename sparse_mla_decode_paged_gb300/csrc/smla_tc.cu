@@ -82,7 +82,7 @@ struct Misc {
   alignas(16) float m_used[kHeads];
   alignas(16) float alpha[kHeads];
   float lse_out[kHeads];
-  float linv[kHeads];
+  alignas(16) float linv[kHeads];
   unsigned char valid[kTile];
 };
 
@@ -195,6 +195,7 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
     constexpr int h2 = H2;                     // latent dims [256 h2, 256 h2 + 256)
     const int t = 32 * quad + lane;            // token within the tile = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * quad) << 16;
+    const unsigned char* kt = reinterpret_cast<const unsigned char*>(__cvta_shared_to_generic(k_base));
     const int seq_len = __ldg(p.seq_lens + b);
     const int32_t* bt_row = p.block_table + (size_t)b * p.max_pages;
     const int32_t* tk_row = p.topk + (size_t)b * p.topk_n;
@@ -298,8 +299,8 @@ __device__ __forceinline__ void gather_role(const SplitParams& p, Misc& ms, vola
         for (int u = 0; u < 8; ++u) {
           const int c = 2 * (2 * h2 + jj) + (u >> 2);
           const uint32_t cb = k_base + c * kKChunkBytes;
-          const uint4 h0 = ptx::lds128(cb + swz(t, 2 * (u & 3)));
-          const uint4 h1 = ptx::lds128(cb + swz(t, 2 * (u & 3) + 1));
+          const uint4 h0 = *reinterpret_cast<const uint4*>(kt + (cb - k_base) + swz(t, 2 * (u & 3)));
+          const uint4 h1 = *reinterpret_cast<const uint4*>(kt + (cb - k_base) + swz(t, 2 * (u & 3) + 1));
           const uint32_t hv[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
           uint32_t lo[8];
 #pragma unroll
@@ -395,19 +396,19 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
       const uint16_t* qg = p.q + ((size_t)b * p.H + (size_t)g * kHeads) * kDQK;
 #pragma unroll 1
-      for (int k0 = 0; k0 < 36; k0 += 9) {
-        uint4 v[9];
+      for (int k0 = 0; k0 < 36; k0 += 18) {
+        uint4 v[18];
 #pragma unroll
-        for (int k = 0; k < 9; ++k) {
+        for (int k = 0; k < 18; ++k) {
           const int id = t + kSoftmaxThreads * (k0 + k);
           const int n = id / 72, j = id % 72;
           v[k] = n < hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int k = 0; k < 9; ++k) {
+        for (int k = 0; k < 18; ++k) {
           const int id = t + kSoftmaxThreads * (k0 + k);
           const int n = id / 72, j = id % 72;
-          ptx::sts128(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
+          ptx::sts128_async_only(q_base + (j >> 3) * kQChunkBytes + swz(n, j & 7), bf8_to_h8(v[k], range_bad));
         }
       }
       ptx::fence_proxy_async_smem();
@@ -517,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
           s[h + 1] = (m[2 * q + 1] == -CUDART_INF_F) ? 0.f : ptx::ex2_approx(s[h + 1] - m[2 * q + 1]);
           w[q] = f32x2_to_f16x2_sat(s[h], s[h + 1]);
         }
-        ptx::sts128(p_base + swz(t, u), make_uint4(w[0], w[1], w[2], w[3]));
+        ptx::sts128_async_only(p_base + swz(t, u), make_uint4(w[0], w[1], w[2], w[3]));
       }
       const float2 ps = reduce_scatter64<false>(s, lane);
       lsum0 = lsum0 * ms.alpha[2 * lane] + ps.x;
@@ -584,24 +585,30 @@ __global__ void __launch_bounds__(kThreads, 1) split_tc_kernel(const SplitParams
       // O / l staged as rows [head][512] (bf16 or fp32) over the K tile, which every MMA has finished
       // reading, then one bulk copy per head row
       const uint32_t elem = p.final_out ? 2u : 4u, row_bytes = 512u * elem;
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t d = 128u * j + t;
+      unsigned char* stage = base + kQBytes;
+      for (int hh = 0; hh < 2; ++hh) {
+        float li[32];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int q = 0; q < 32; q += 4) {
+          const float4 v = reinterpret_cast<const float4*>(ms.linv)[(32 * hh + q) / 4];
+          li[q] = v.x; li[q + 1] = v.y; li[q + 2] = v.z; li[q + 3] = v.w;
+        }
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t d = 128u * j + t;
           uint32_t r[32];
           ptx::tmem_ld32(tmem + lane_base + 64 * j + 32 * hh, r);
           ptx::tmem_wait_ld();
+          if (p.final_out) {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) {
-            const uint32_t hl = 32 * hh + q;
-            const float o = __uint_as_float(r[q]) * ms.linv[hl];
-            const uint32_t sa = k_base + hl * row_bytes + d * elem;
-            if (p.final_out) {
-              const uint16_t v = (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
-              asm volatile("st.shared.u16 [%0], %1;" ::"r"(sa), "h"(v) : "memory");
-            } else {
-              asm volatile("st.shared.f32 [%0], %1;" ::"r"(sa), "f"(o) : "memory");
+            for (int q = 0; q < 32; ++q) {
+              const float o = __uint_as_float(r[q]) * li[q];
+              *reinterpret_cast<uint16_t*>(stage + (32 * hh + q) * row_bytes + d * 2) =
+                  (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu);
             }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              *reinterpret_cast<float*>(stage + (32 * hh + q) * row_bytes + d * 4) = __uint_as_float(r[q]) * li[q];
           }
         }
       }
