@@ -458,7 +458,21 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", type=int, default=0,
+                    help="profiling driver: run this many eager calls of --workload (optionally --nsplit) and exit")
+    ap.add_argument("--nsplit", type=int, default=0)
     args = ap.parse_args()
+    if args.single:
+        import torch
+        from sparse_mla_decode_paged_gb300 import api
+        from sparse_mla_decode_paged_gb300 import workloads as wl
+        w = wl.make_workload(wl.CONFIGS[args.workload], device="cuda")
+        for _ in range(args.single):
+            api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                  nsplit=args.nsplit)
+        torch.cuda.synchronize()
+        print("ok")
+        return
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
