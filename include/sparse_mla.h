@@ -179,6 +179,31 @@ int sparse_mla_read_errors(const void* workspace, uint32_t* flags, smla_stream_t
 /* Static description of a status code. */
 const char* sparse_mla_status_string(int status);
 
+/* Decode that allocates nothing and needs no workspace argument.  The pages
+ * have no counterpart: it exists for callers that cannot allocate device
+ * memory -- plugins hosted by an engine that owns the whole device pool and
+ * hands out no workspace, code running while a stream is being captured into
+ * a CUDA graph, host paths that must not risk cudaMalloc's implicit device
+ * synchronisation.  Same inputs, outputs and kernels as sparse_mla_decode;
+ * the split partials and the device error word live in a file-scope device
+ * array of 32 MiB (SMLA_NOALLOC_SCRATCH_BYTES) that every GPU loading the
+ * library holds until the process exits.
+ *   - The first call on a device looks the array's device address up
+ *     (cudaGetSymbolAddress, once per device, with that device current); make
+ *     that first call before any stream capture on the device.
+ *   - Shapes whose partials do not fit (sparse_mla_workspace_size > 32 MiB for
+ *     the chosen nsplit) return SMLA_ERR_WORKSPACE and enqueue nothing; use
+ *     sparse_mla_decode with a caller workspace or a smaller nsplit then.
+ *   - No cudaMalloc, cudaFree or allocating library call is made.
+ *   - Every call shares the array and leaves its contents behind: the error
+ *     word is cleared at the start of each call (it is not readable through
+ *     this API), and calls that overlap on the GPU (other streams, other
+ *     threads) race on the array and must be ordered by the caller. */
+#define SMLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int sparse_mla_decode_noalloc(const smla_dims* dims, const void* q, const void* kv_cache,
+                              const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
+                              float sm_scale, void* out, float* lse, smla_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
