@@ -68,6 +68,15 @@ def aggregate_us_per_call(max_elapsed_s: float, steps: int, world: int) -> float
     return max_elapsed_s * 1e6 / (steps * world)
 
 
+def replica_spec(name: str, rank: int):
+    """The workload recipe a replica runs: the named configuration with a seed of its own per rank
+    (rank 0 keeps the configuration's seed), so replicas read different rows of their caches."""
+    import dataclasses
+    from sparse_mla_decode_paged_gb300 import workloads as wl
+    spec = wl.CONFIGS[name]
+    return dataclasses.replace(spec, seed=spec.seed + 7777 * rank) if rank else spec
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -162,10 +171,7 @@ class Bench:
         from sparse_mla_decode_paged_gb300 import workloads as wl
         self.torch, self.api, self.wl = torch, api, wl
         self.name = name
-        spec = wl.CONFIGS[name]
-        if seed_offset:
-            import dataclasses
-            spec = dataclasses.replace(spec, seed=spec.seed + 7777 * seed_offset)
+        spec = replica_spec(name, seed_offset)
         self.spec = spec
         self.device = device
         w0 = wl.make_workload(spec, device=device, pool_pages=MIN_POOL_PAGES)
