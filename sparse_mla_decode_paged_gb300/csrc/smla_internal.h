@@ -39,8 +39,7 @@ struct SplitParams {
 };
 
 // Kernel launchers (return the launch error).
-cudaError_t launch_split_tc(const SplitParams& p, cudaStream_t stream);
-cudaError_t launch_split_simt(const SplitParams& p, cudaStream_t stream);
+cudaError_t launch_split_pair(const SplitParams& p, cudaStream_t stream);
 size_t workspace_bytes_for(int B, int H, int nsplit);
 cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part,
                            uint16_t* out, float* lse, cudaStream_t stream);
@@ -52,7 +51,9 @@ cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int
 bool split_shape_supported(int H, int topk);
 // Resident CTAs per SM of the split kernel for H heads (occupancy of its smem/threads).
 int split_ctas_per_sm(int H);
-// Heads handled by one CTA of the split kernel (H is split into ceil(H / this) groups).
+// Heads handled by one work unit of the split kernel (H is split into ceil(H / this) groups).
 int split_heads_per_cta();
+// CTAs per work unit (one unit per query, partition and head group): a cluster of this many CTAs.
+int split_ctas_per_unit();
 
 }  // namespace smla

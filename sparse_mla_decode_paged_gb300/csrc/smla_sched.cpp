@@ -57,7 +57,7 @@ static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit
                           int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
   const int hpc = split_heads_per_cta();
   const int head_groups = (H + hpc - 1) / hpc;
-  const int ctas = B * head_groups * nsplit;
+  const int ctas = B * head_groups * nsplit * split_ctas_per_unit();
   const double slots = (double)sm_count * ctas_per_sm;
   const double waves = ctas / slots;
   const int whole_waves = (int)ceil(waves - 1e-9);
