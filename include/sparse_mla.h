@@ -93,8 +93,8 @@ typedef struct smla_plan {
   int32_t nsplit;             /* partitions of the top-k list                            */
   int32_t tokens_per_split;   /* top-k entries per partition (last may be shorter)       */
   int32_t head_groups;        /* groups of 64 heads per (query, partition)               */
-  int32_t ctas;               /* grid size of the split kernel: 2 CTAs (a cluster) per   */
-                              /* (query, partition, head group)                          */
+  int32_t ctas;               /* grid size of the split kernel: one CTA per (query,      */
+                              /* partition, head group)                                  */
   int32_t ctas_per_sm;        /* CTAs of the split kernel resident per SM                */
   int32_t sm_count;           /* SMs the plan was made for                               */
   double waves;               /* ctas / (sm_count * ctas_per_sm)                         */

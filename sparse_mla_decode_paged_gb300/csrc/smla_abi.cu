@@ -81,7 +81,7 @@ extern "C" int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const voi
   p.lse_part = lse_part;
   p.err = err_word;
   p.final_out = false;
-  return launch_split_pair(p, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  return launch_split(p, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
 extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const void* kv_cache,
@@ -117,7 +117,7 @@ extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const voi
     p.o_part = reinterpret_cast<float*>(ws + kWorkspaceHeader + lse_bytes);
   }
   cudaStream_t s = (cudaStream_t)stream;
-  if (launch_split_pair(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (launch_split(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
   if (nsplit > 1 &&
       launch_combine(dims->batch, dims->num_heads, nsplit, p.o_part, p.lse_part, p.out, lse, s) != cudaSuccess)
     return SMLA_ERR_CUDA;

@@ -39,7 +39,7 @@ struct SplitParams {
 };
 
 // Kernel launchers (return the launch error).
-cudaError_t launch_split_pair(const SplitParams& p, cudaStream_t stream);
+cudaError_t launch_split(const SplitParams& p, cudaStream_t stream);
 size_t workspace_bytes_for(int B, int H, int nsplit);
 cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part,
                            uint16_t* out, float* lse, cudaStream_t stream);
@@ -53,7 +53,7 @@ bool split_shape_supported(int H, int topk);
 int split_ctas_per_sm(int H);
 // Heads handled by one work unit of the split kernel (H is split into ceil(H / this) groups).
 int split_heads_per_cta();
-// CTAs per work unit (one unit per query, partition and head group): a cluster of this many CTAs.
+// CTAs per work unit (one unit per query, partition and head group).
 int split_ctas_per_unit();
 
 }  // namespace smla

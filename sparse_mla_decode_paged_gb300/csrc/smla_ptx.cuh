@@ -123,6 +123,15 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
 }
 
+// mbar_wait_bounded for a whole warp: every lane polls (measured faster than one polling lane that
+// broadcasts its verdict) and the verdict is the AND over the lanes.  All 32 lanes must call it.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort, int lane,
+                                               uint64_t limit_ns = 1000000000ull) {
+  (void)lane;
+  const bool ok = mbar_wait_bounded(bar, parity, abort, limit_ns);
+  return __all_sync(0xffffffffu, ok);
+}
+
 // ----------------------------------------------------------------------------- proxies / barriers
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -275,13 +284,27 @@ __host__ __device__ constexpr uint32_t idesc_f16(uint32_t m, uint32_t n, uint32_
 
 // ----------------------------------------------------------------------------- loads
 
-// 16-byte streaming load through the non-coherent path, not kept in L1.
+// 16-byte streaming load through the non-coherent path, not kept in L1.  Volatile, so that it is
+// issued where it is written (a prefetch), not moved down to the first use of its result.
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
   uint4 v;
-  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// 32-bit load through the non-coherent path, issued where it is written (see ldg_stream).
+__device__ __forceinline__ int ldg_i32_now(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.nc.s32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 (TMA engine; no
+// registers or L1 space are used and nothing waits for it).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Bulk copy shared -> global (TMA engine), tracked by the issuing thread's bulk groups.

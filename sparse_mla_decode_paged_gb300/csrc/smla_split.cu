@@ -1,0 +1,697 @@
+// Split kernel (sm_103a): tcgen05 MMAs with TMEM accumulators, exact scores.
+//
+// One CTA per (partition s of the top-k list, group of 64 heads, query b); the
+// partition is walked in tiles of 128 top-k entries (MMA M = 128 tokens,
+// N = 64 heads).  ("The 64-Block Barrier", "The Split-K Prescription":
+// dequantise, QK^T over 576 dims, online softmax, PV over 512 dims, split-K.)
+//
+// Numerics.  A block scale is split as sc = mant * 2^e with mant in [1, 2)
+// (e clamped to [-15, 7]).  The K tile holds K' = code * 2^e in fp16, exact
+// for every E4M3 code, and Q is fp16 (exact for bf16 inside the fp16 range),
+// so each 128-dim block's MMA S_b = K'_b . Q_b^T is exact up to fp32
+// accumulation; the softmax warps form  s = sum_b mant_b * S_b + S_rope  in
+// fp32 as the four block accumulators complete.  PV reads the same K' with the
+// mantissa moved onto the probabilities:  O_b^T += K'_b^T . (P * mant_b), the
+// products P * mant_b rounded to fp16.
+//
+// Warp roles (12 warps, one CTA per SM):
+//   gather (8 warps)   warp g owns tokens [16g, 16g + 16) of a tile.  Lanes
+//                      0..15 resolve index -> row through the block table
+//                      (a1) as a three-stage pipeline: the top-k entries of
+//                      tile i + 2, the block-table entries of tile i + 1 and
+//                      the record bytes of tile i + 1 are in flight while tile
+//                      i is converted (all issued where they are written, so
+//                      no load waits on another).  The record bytes are read
+//                      coalesced: one token's 512 code bytes per warp load,
+//                      four tokens' rope bytes, sixteen tokens' scales.  Codes
+//                      -> K' (fp16, 128B-swizzled chunks of 64 dims), rope
+//                      bf16 -> fp16, mantissas and validity to shared memory.
+//                      A warp signals its part of the tile (mbarrier) before
+//                      it issues the next loads: a fence or barrier after them
+//                      would wait for them.
+//   MMA issue          thread 0 (a softmax thread, which has no loads in
+//                      flight): QK block b into score buffer b (b = 0..3), the
+//                      rope into buffer 0 once block 0 has been read out, and
+//                      the PV MMAs.
+//   softmax (4 warps)  one token (TMEM lane) per thread, 64 heads: scores
+//                      accumulated from the score buffers as they complete,
+//                      lazy running max (a head's reference moves only when a
+//                      score exceeds it by more than 2^8; O and the row sums
+//                      are then rescaled), P = exp2(s - m), row sums reduced
+//                      over the warp.  PV runs block by block: P * mant_b is
+//                      written into the rope chunk or chunk 0 of the K tile
+//                      (each free once the MMAs reading it are done: the rope
+//                      QK, resp. the PV of block 0) and thread 0 issues that
+//                      block's 8 MMAs, so writing P * mant_{b+1} overlaps PV
+//                      of block b.
+//   epilogue (all)     O / l from TMEM straight to global memory, lse.
+//
+// Shared memory: Q 72 KB + K tile 144 KB + ~4 KB; TMEM: O^T in columns
+// 0..255 (4 blocks x 64 heads), score buffers in 256..511.
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "smla_device.cuh"
+#include "smla_ptx.cuh"
+
+namespace smla {
+namespace {
+
+constexpr int kTile = 128;
+constexpr int kHeads = 64;
+constexpr int kThreads = 384;
+constexpr int kSoftWarps = 4;
+constexpr int kSoftThreads = 32 * kSoftWarps;     // warps 0..3: TMEM lane quadrants 0..3
+constexpr int kGatherWarps = 8;
+constexpr int kTokPerGatherWarp = kTile / kGatherWarps;   // 16
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kSCol = 256;                   // score buffer b at 256 + 64 b
+constexpr float kRescaleThreshold = 8.0f;         // log2 units: P <= 2^8
+constexpr float kFp16Max = 65504.0f;
+constexpr float kMaxScale = 16384.0f;             // P * mant <= 2^8 * 2^7 stays inside fp16
+
+constexpr uint32_t kQChunk = kHeads * 128;        // 64 heads x 64 dims fp16
+constexpr uint32_t kKChunk = kTile * 128;         // 128 tokens x 64 dims fp16
+constexpr uint32_t kQBytes = 9 * kQChunk;         // 73728
+constexpr uint32_t kKBase = kQBytes;
+constexpr uint32_t kKBytes = 9 * kKChunk;         // 147456
+constexpr uint32_t kRopeChunk = 8;
+constexpr uint32_t kMiscOff = kKBase + kKBytes;
+
+constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kHeads, 0, 0);
+constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
+
+struct Misc {
+  uint64_t q_ready;          // Q staged (one arrival per softmax warp)
+  uint64_t tile_full;        // K tile and metadata of the tile written (one arrival per gather warp)
+  uint64_t s_full[4];        // score buffer b holds block b of the tile
+  uint64_t s_free0;          // buffer 0 read out (one arrival per softmax warp): the rope may go there
+  uint64_t r_full;           // buffer 0 holds the rope scores
+  uint64_t pv0_done, pv1_done;
+  uint64_t pv_done;          // every PV MMA of the tile complete: the K tile is free
+  uint64_t teardown;         // every MMA complete
+  uint32_t tmem_slot;
+  int abort;
+  int range_err;
+  alignas(16) float mant[4][kTile];
+  unsigned char valid[kTile];
+  alignas(16) float m_ref[kHeads];       // reference max per head, log2 units
+  alignas(16) float m_new[kHeads];
+  alignas(16) float alpha[kHeads];
+  alignas(16) float red[kSoftWarps][kHeads];
+  alignas(16) float linv[kHeads];
+  float lse_out[kHeads];
+};
+
+constexpr size_t kSmemBytes = 1024 + kMiscOff + sizeof(Misc);
+static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
+  return row * 128u + ((unit ^ (row & 7u)) << 4);
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// sc = mant * 2^e, e = clamp(exponent(sc), -15, 7); returns mant (exact) and 2^e as fp16 bits.
+__device__ __forceinline__ float pow2_split(float sc, uint32_t& p2) {
+  const uint32_t bits = __float_as_uint(sc) & 0x7fffffffu;
+  int e = (int)(bits >> 23) - 127;
+  e = max(-15, min(7, e));
+  const float mant = sc * __uint_as_float((uint32_t)(127 - e) << 23);
+  p2 = e >= -14 ? (uint32_t)(e + 15) << 10 : 0x0200u;   // 2^-15 is an fp16 subnormal
+  return mant;
+}
+
+// 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
+__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, int& range_bad) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+  range_bad |= (fabsf(lo) > kFp16Max) | (fabsf(hi) > kFp16Max);
+  return f32x2_to_f16x2_sat(lo, hi);
+}
+
+__device__ __forceinline__ uint4 bf8_to_h8(uint4 v, int& range_bad) {
+  return make_uint4(bf2_to_h2(v.x, range_bad), bf2_to_h2(v.y, range_bad), bf2_to_h2(v.z, range_bad),
+                    bf2_to_h2(v.w, range_bad));
+}
+
+__device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
+  const int lo = __shfl_sync(0xffffffffu, (int)(v & 0xffffffff), src);
+  const int hi = __shfl_sync(0xffffffffu, (int)(v >> 32), src);
+  return (int64_t)(((uint64_t)(uint32_t)hi << 32) | (uint32_t)lo);
+}
+
+// Warp reduce-scatter over 64 per-thread values: afterwards lane l holds the reduction over the
+// warp's 32 threads of columns 2l and 2l+1 (62 shuffles; v is kept).
+template <bool kMax>
+__device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lane) {
+  float a[32];
+  {
+    const bool hi = lane & 16;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float send = hi ? v[i] : v[32 + i];
+      const float keep = hi ? v[32 + i] : v[i];
+      const float r = __shfl_xor_sync(0xffffffffu, send, 16);
+      a[i] = kMax ? fmaxf(keep, r) : keep + r;
+    }
+  }
+#pragma unroll
+  for (int span = 16, x = 8; span >= 2; span >>= 1, x >>= 1) {
+    const bool hi = lane & x;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      if (i < span) {
+        const float send = hi ? a[i] : a[span + i];
+        const float keep = hi ? a[span + i] : a[i];
+        const float r = __shfl_xor_sync(0xffffffffu, send, x);
+        a[i] = kMax ? fmaxf(keep, r) : keep + r;
+      }
+    }
+  }
+  return make_float2(a[0], a[1]);
+}
+
+struct Ctx {
+  const SplitParams* p;
+  Misc* ms;
+  volatile int* abort;
+  uint32_t q_base, k_base;   // shared addresses
+  uint32_t tmem;
+  int b, g, split, pos0, pos_end, n_tiles, hg_valid;
+};
+
+// ------------------------------------------------------------------------------------------ gather
+__device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
+  const SplitParams& p = *x.p;
+  Misc& ms = *x.ms;
+  const int gw = warp - kSoftWarps;
+  const int tl = kTokPerGatherWarp * gw + (lane & 15);   // token resolved by this lane (lanes 16.. repeat)
+  const int seq_len = __ldg(p.seq_lens + x.b);
+  const int32_t* bt_row = p.block_table + (size_t)x.b * p.max_pages;
+  const int32_t* tk_row = p.topk + (size_t)x.b * p.topk_n;
+  const unsigned char* kv = p.kv;
+  const int blk = lane >> 3;               // scale block of this lane's 16 latent dims
+  int range_bad = 0;
+  bool ok = true;
+
+  // Index -> row (a1) in three stages.  A top-k entry t is used when 0 <= t < seq_len; its
+  // logical page t / 64 must lie in the block-table row and the physical page in the cache, else
+  // the entry is skipped and flagged.
+  auto topk_load = [&](int j) -> int {
+    const int pos = x.pos0 + j * kTile + tl;
+    return (j < x.n_tiles && pos < x.pos_end) ? ptx::ldg_i32_now(tk_row + pos) : -1;
+  };
+  auto page_load = [&](int t) -> int {      // block-table entry of t, or 0 when t is not looked up
+    const bool used = t >= 0 && t < seq_len && (t >> 6) < p.max_pages;
+    return used ? ptx::ldg_i32_now(bt_row + (t >> 6)) : 0;
+  };
+  auto row_from = [&](int t, int page) -> int64_t {
+    if (t < 0 || t >= seq_len) return -1;
+    if ((t >> 6) >= p.max_pages || page < 0 || (int64_t)page >= p.num_pages) {
+      if (p.err) atomicOr(p.err, SMLA_DEVERR_PAGE_RANGE);
+      return -1;
+    }
+    return (int64_t)page * kPageSize + (t & (kPageSize - 1));
+  };
+
+  // Record bytes of the warp's 16 tokens: load k reads token 16 gw + k's 512 code bytes (one
+  // contiguous segment per warp load, lane l: dims 16 l .. 16 l + 15); rope: four tokens x 128
+  // bytes per load; scales: lanes 0..15, one token each.
+  uint4 lat[16], rope[4], sc;
+  auto load_tile = [&](int64_t r_own) {
+    const int64_t off_own = r_own >= 0 ? r_own * kRecordBytes : -1;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const int64_t off = shfl_i64(off_own, k);
+      lat[k] = off >= 0 ? ptx::ldg_stream(kv + off + 16 * lane) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t off = shfl_i64(off_own, 4 * k + (lane >> 3));
+      rope[k] = off >= 0 ? ptx::ldg_stream(kv + off + 528 + 16 * (lane & 7)) : make_uint4(0, 0, 0, 0);
+    }
+    sc = off_own >= 0 ? ptx::ldg_stream(kv + off_own + 512) : make_uint4(0, 0, 0, 0);
+  };
+
+  // prologue: tile 0 resolved and its records in flight; tile 1's page and tile 2's entries in flight
+  const int t0 = topk_load(0);
+  int t1 = topk_load(1);
+  int64_t row = row_from(t0, page_load(t0));
+  load_tile(row);
+  int pg1 = page_load(t1);
+  int t2 = topk_load(2);
+
+  for (int i = 0; i < x.n_tiles; ++i) {
+    const bool valid = row >= 0;
+    // the K tile is free once every PV MMA of the previous tile is done
+    if (i > 0) ok = ptx::mbar_wait_warp(&ms.pv_done, (i - 1) & 1, x.abort, lane) && ok;
+    if (ok) {
+      const float s4[4] = {__uint_as_float(sc.x), __uint_as_float(sc.y), __uint_as_float(sc.z),
+                           __uint_as_float(sc.w)};
+      uint32_t e[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float mt = pow2_split(s4[q], e[q]);
+        if (lane < 16) ms.mant[q][tl] = valid ? mt : 0.f;
+        if (valid) range_bad |= !(fabsf(s4[q]) <= kMaxScale);
+      }
+      if (lane < 16) ms.valid[tl] = valid;
+      const uint32_t e01 = e[0] | (e[1] << 16), e23 = e[2] | (e[3] << 16);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t a01 = __shfl_sync(0xffffffffu, e01, k), a23 = __shfl_sync(0xffffffffu, e23, k);
+        const uint32_t pair = blk < 2 ? a01 : a23;
+        const uint32_t h = (blk & 1) ? (pair >> 16) : (pair & 0xFFFFu);
+        const uint32_t m2 = h | (h << 16);
+        const uint32_t w[4] = {lat[k].x, lat[k].y, lat[k].z, lat[k].w};
+        uint32_t hv[8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          hv[2 * q] = hmul2(e4m3x2_to_f16x2((uint16_t)(w[q] & 0xFFFFu)), m2);
+          hv[2 * q + 1] = hmul2(e4m3x2_to_f16x2((uint16_t)(w[q] >> 16)), m2);
+        }
+        const uint32_t t = kTokPerGatherWarp * gw + k;
+        const uint32_t cb = x.k_base + (lane >> 2) * kKChunk;
+        const uint32_t u0 = 2 * (lane & 3), sw = (lane >> 2) & 1;
+        const uint4 lo4 = make_uint4(hv[0], hv[1], hv[2], hv[3]), hi4 = make_uint4(hv[4], hv[5], hv[6], hv[7]);
+        // units u0, u0 + 1 in an order that keeps every 8 lanes of a store on distinct banks
+        ptx::sts128_async_only(cb + swz128(t, u0 + sw), sw ? hi4 : lo4);
+        ptx::sts128_async_only(cb + swz128(t, u0 + 1 - sw), sw ? lo4 : hi4);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t t = kTokPerGatherWarp * gw + 4 * k + (lane >> 3);
+        ptx::sts128_async_only(x.k_base + kRopeChunk * kKChunk + swz128(t, lane & 7), bf8_to_h8(rope[k], range_bad));
+      }
+    }
+    // the tile is written: signal it, and only then put the next loads in flight (a fence or a
+    // barrier after them would wait for them)
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms.tile_full);
+    // tile i + 1's records, tile i + 2's pages, tile i + 3's entries
+    row = row_from(t1, pg1);
+    if (i + 1 < x.n_tiles) load_tile(row);
+    pg1 = page_load(t2);
+    t1 = t2;
+    t2 = topk_load(i + 3);
+  }
+  if (range_bad) ms.range_err = 1;
+}
+
+// ------------------------------------------------------------------------------------------ softmax
+__device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
+  const SplitParams& p = *x.p;
+  Misc& ms = *x.ms;
+  const int t = threadIdx.x;                 // token of the tile = TMEM lane
+  const bool issuer = (t == 0);              // every MMA
+  const uint32_t lane_q = (uint32_t)(32 * warp) << 16;
+  int range_bad = 0;
+  bool ok = true, mma_ok = true;
+
+  {
+    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
+    const uint16_t* qg = p.q + ((size_t)x.b * p.H + (size_t)x.g * kHeads) * kDQK;
+#pragma unroll 1
+    for (int k0 = 0; k0 < 36; k0 += 18) {
+      uint4 v[18];
+#pragma unroll
+      for (int k = 0; k < 18; ++k) {
+        const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
+        v[k] = n < x.hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j)
+                              : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < 18; ++k) {
+        const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
+        ptx::sts128_async_only(x.q_base + (j >> 3) * kQChunk + swz128(n, j & 7), bf8_to_h8(v[k], range_bad));
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(&ms.q_ready);
+  }
+
+  const float c2 = p.sm_scale * 1.4426950408889634f;
+  float lsum0 = 0.f, lsum1 = 0.f;            // this warp's row sums of heads 2 lane, 2 lane + 1
+  const uint32_t bufR = x.k_base + kRopeChunk * kKChunk, buf0 = x.k_base;
+
+  for (int i = 0; i < x.n_tiles; ++i) {
+    const uint32_t ph = i & 1;
+    ok = ptx::mbar_wait_warp(&ms.tile_full, ph, x.abort, lane) && ok;
+    if (issuer) {
+      // QK of the four latent blocks, block b into score buffer b
+      if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_bounded(&ms.q_ready, 0, x.abort);
+      mma_ok = mma_ok && ok;
+      if (mma_ok) {
+        ptx::tc_fence_after();
+#pragma unroll 1
+        for (int bb = 0; bb < 4; ++bb) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int ch = 2 * bb + cc;
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_f16_ss(x.tmem + kSCol + 64 * bb, ptx::sw128_desc(x.k_base + ch * kKChunk + 32 * kk, 16, 1024),
+                              ptx::sw128_desc(x.q_base + ch * kQChunk + 32 * kk, 16, 1024), kIdescQK,
+                              (cc | kk) != 0);
+          }
+          ptx::mma_commit(&ms.s_full[bb]);
+        }
+      }
+    }
+    __syncwarp();
+    const bool valid = ms.valid[t];
+    float mant[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mant[q] = ms.mant[q][t];
+    float s[64];
+#pragma unroll
+    for (int h = 0; h < 64; ++h) s[h] = 0.f;
+    // scores: block buffers as they complete, then the rope
+#pragma unroll 1
+    for (int bb = 0; bb < 5; ++bb) {
+      ok = ptx::mbar_wait_warp(bb < 4 ? &ms.s_full[bb] : &ms.r_full, ph, x.abort, lane) && ok;
+      if (ok) {
+        ptx::tc_fence_after();
+        const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : bb == 3 ? mant[3] : 1.f);
+        const uint32_t sa = x.tmem + lane_q + kSCol + 64 * (bb < 4 ? bb : 0);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t r[32];
+          ptx::tmem_ld32(sa + 32 * hh, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) s[32 * hh + h] = fmaf(f, __uint_as_float(r[h]), s[32 * hh + h]);
+        }
+      }
+      if (bb == 0) {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&ms.s_free0);
+        if (issuer) {
+          // the rope scores go to buffer 0 once every warp has read block 0 out of it
+          mma_ok = mma_ok && ptx::mbar_wait_bounded(&ms.s_free0, ph, x.abort);
+          if (mma_ok) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              ptx::mma_f16_ss(x.tmem + kSCol,
+                              ptx::sw128_desc(x.k_base + kRopeChunk * kKChunk + 32 * kk, 16, 1024),
+                              ptx::sw128_desc(x.q_base + kRopeChunk * kQChunk + 32 * kk, 16, 1024), kIdescQK,
+                              kk != 0);
+            ptx::mma_commit(&ms.r_full);
+          }
+        }
+        __syncwarp();
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 64; ++h) s[h] = (ok && valid) ? s[h] : -CUDART_INF_F;
+    bool need = false;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
+      need |= (s[4 * k] > m.x + kRescaleThreshold) | (s[4 * k + 1] > m.y + kRescaleThreshold) |
+              (s[4 * k + 2] > m.z + kRescaleThreshold) | (s[4 * k + 3] > m.w + kRescaleThreshold);
+    }
+    need = ptx::named_bar_or(3, kSoftThreads, need);
+    if (need) {
+      // a head's reference max moves to its tile max when that exceeds it by more than the threshold
+      const float2 mx = reduce_scatter64<true>(s, lane);
+      ms.red[warp][2 * lane] = mx.x;
+      ms.red[warp][2 * lane + 1] = mx.y;
+      ptx::named_bar_sync(2, kSoftThreads);
+      if (warp == 0) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int h = 2 * lane + e;
+          const float tm = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+          const float mo = ms.m_ref[h];
+          const float mn = tm > mo + kRescaleThreshold ? tm : mo;
+          ms.alpha[h] = mo == -CUDART_INF_F ? 0.f : ptx::ex2_approx(mo - mn);
+          ms.m_new[h] = mn;
+        }
+      }
+      ptx::named_bar_sync(2, kSoftThreads);
+      lsum0 *= ms.alpha[2 * lane];
+      lsum1 *= ms.alpha[2 * lane + 1];
+      if (i > 0 && ok) {
+        // O of the previous tiles (their PV is complete: this tile's K was written after it)
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t r[32];
+          const uint32_t oa = x.tmem + lane_q + 32 * c;
+          ptx::tmem_ld32(oa, r);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int h = 0; h < 32; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * ms.alpha[32 * (c & 1) + h]);
+          ptx::tmem_st32(oa, r);
+        }
+        ptx::tmem_wait_st();
+      }
+      ptx::named_bar_sync(2, kSoftThreads);
+      if (warp == 0) {
+        ms.m_ref[2 * lane] = ms.m_new[2 * lane];
+        ms.m_ref[2 * lane + 1] = ms.m_new[2 * lane + 1];
+      }
+      ptx::named_bar_sync(2, kSoftThreads);
+    }
+    // P = exp2(s - m) (a head with no valid entry yet has m = -inf and P = 0), fp16 pairs
+    uint32_t ph2[32];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
+      const float mm[4] = {m.x, m.y, m.z, m.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int h = 4 * k + q;
+        s[h] = mm[q] == -CUDART_INF_F ? 0.f : ptx::ex2_approx(s[h] - mm[q]);
+      }
+      ph2[2 * k] = f32x2_to_f16x2_sat(s[4 * k], s[4 * k + 1]);
+      ph2[2 * k + 1] = f32x2_to_f16x2_sat(s[4 * k + 2], s[4 * k + 3]);
+    }
+    const float2 ps = reduce_scatter64<false>(s, lane);
+    lsum0 += ps.x;
+    lsum1 += ps.y;
+
+    // PV block by block: P * mant_b into the rope chunk (b = 0, 2) or chunk 0 (b = 1, 3), each free
+    // once the MMAs reading it are done (the rope QK, resp. the PV of block 0)
+    auto write_pm = [&](int bb, uint32_t buf) {
+      const float mb = bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : mant[3];
+      const uint32_t m2 = f32x2_to_f16x2_sat(mb, mb);
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        ptx::sts128_async_only(buf + swz128(t, u), make_uint4(hmul2(ph2[4 * u], m2), hmul2(ph2[4 * u + 1], m2),
+                                                              hmul2(ph2[4 * u + 2], m2), hmul2(ph2[4 * u + 3], m2)));
+    };
+    auto issue_pv = [&](int bb, uint32_t buf) {
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk)
+        ptx::mma_f16_ss(x.tmem + 64 * bb, ptx::sw128_desc(x.k_base + 2 * bb * kKChunk + kk * 2048, kKChunk, 1024),
+                        // P spans one 64-head atom along N: its leading offset is never stepped
+                        ptx::sw128_desc(buf + kk * 2048, 1024, 1024), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+    };
+    write_pm(0, bufR);
+    ptx::fence_proxy_async_smem();
+    ptx::tc_fence_before();
+    ptx::named_bar_sync(2, kSoftThreads);
+    if (issuer) {
+      mma_ok = mma_ok && ok;
+      if (mma_ok) {
+        ptx::tc_fence_after();
+        issue_pv(0, bufR);
+        ptx::mma_commit(&ms.pv0_done);
+      }
+    }
+    ok = ptx::mbar_wait_warp(&ms.pv0_done, ph, x.abort, lane) && ok;
+    write_pm(1, buf0);
+    write_pm(2, bufR);
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(2, kSoftThreads);
+    if (issuer && mma_ok) {
+      ptx::tc_fence_after();
+      issue_pv(1, buf0);
+      ptx::mma_commit(&ms.pv1_done);
+      issue_pv(2, bufR);
+    }
+    ok = ptx::mbar_wait_warp(&ms.pv1_done, ph, x.abort, lane) && ok;
+    write_pm(3, buf0);
+    ptx::fence_proxy_async_smem();
+    ptx::named_bar_sync(2, kSoftThreads);
+    if (issuer && mma_ok) {
+      ptx::tc_fence_after();
+      issue_pv(3, buf0);
+      ptx::mma_commit(&ms.pv_done);
+    }
+  }
+  if (range_bad) ms.range_err = 1;
+  if (issuer) ptx::mma_commit(&ms.teardown);
+  ms.red[warp][2 * lane] = lsum0;
+  ms.red[warp][2 * lane + 1] = lsum1;
+}
+
+// ------------------------------------------------------------------------------------------ epilogue
+// All 12 warps: warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and
+// the 32-column chunks c = w / 4, w / 4 + 3, ... of O^T (chunk c: block c / 2, heads 32 (c % 2) ..).
+__device__ __forceinline__ void epilogue(const Ctx& x, int warp, int lane, bool ok) {
+  const SplitParams& p = *x.p;
+  Misc& ms = *x.ms;
+  if (!ok) return;
+  const int quad = warp & 3;
+  const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
+  for (int c = warp >> 2; c < 8; c += 3) {
+    const int jb = c >> 1, hb = 32 * (c & 1);
+    uint32_t r[32];
+    ptx::tmem_ld32(x.tmem + lane_q + 32 * c, r);
+    ptx::tmem_wait_ld();
+    const int d = 128 * jb + 32 * quad + lane;
+    const size_t hrow0 = (size_t)x.g * kHeads + hb;
+    if (p.final_out) {
+      uint16_t* o = p.out + ((size_t)x.b * p.H + hrow0) * kDLatent + d;
+#pragma unroll
+      for (int h = 0; h < 32; ++h)
+        if (hb + h < x.hg_valid)
+          o[(size_t)h * kDLatent] = (uint16_t)(f32x2_to_bf16x2(__uint_as_float(r[h]) * ms.linv[hb + h], 0.f) & 0xFFFFu);
+    } else {
+      float* o = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + hrow0) * kDLatent + d;
+#pragma unroll
+      for (int h = 0; h < 32; ++h)
+        if (hb + h < x.hg_valid) o[(size_t)h * kDLatent] = __uint_as_float(r[h]) * ms.linv[hb + h];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& ms = *reinterpret_cast<Misc*>(base + kMiscOff);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  Ctx x;
+  x.p = &p;
+  x.ms = &ms;
+  x.abort = &ms.abort;
+  x.q_base = ptx::smem_u32(base);
+  x.k_base = x.q_base + kKBase;
+  x.split = blockIdx.x;
+  x.g = blockIdx.y;
+  x.b = blockIdx.z;
+  x.pos0 = x.split * p.split_len;
+  x.pos_end = min(x.pos0 + p.split_len, p.topk_n);
+  x.n_tiles = x.pos_end > x.pos0 ? (x.pos_end - x.pos0 + kTile - 1) / kTile : 0;
+  x.hg_valid = min(kHeads, p.H - kHeads * x.g);
+
+  if (x.n_tiles == 0) {
+    // empty partition: out = 0, lse = -inf
+    for (int i = threadIdx.x; i < x.hg_valid * kDLatent; i += kThreads) {
+      const size_t h = (size_t)x.g * kHeads + i / kDLatent;
+      const int d = i % kDLatent;
+      if (p.final_out) p.out[((size_t)x.b * p.H + h) * kDLatent + d] = 0;
+      else p.o_part[(((size_t)x.b * p.nsplit + x.split) * p.H + h) * kDLatent + d] = 0.f;
+    }
+    if ((int)threadIdx.x < x.hg_valid) {
+      const size_t h = (size_t)x.g * kHeads + threadIdx.x;
+      if (p.final_out) p.lse[(size_t)x.b * p.H + h] = -CUDART_INF_F;
+      else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = -CUDART_INF_F;
+    }
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(&ms.q_ready, kSoftWarps);
+    ptx::mbar_init(&ms.tile_full, kGatherWarps);
+    for (int bb = 0; bb < 4; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
+    ptx::mbar_init(&ms.s_free0, kSoftWarps);
+    ptx::mbar_init(&ms.r_full, 1);
+    ptx::mbar_init(&ms.pv0_done, 1);
+    ptx::mbar_init(&ms.pv1_done, 1);
+    ptx::mbar_init(&ms.pv_done, 1);
+    ptx::mbar_init(&ms.teardown, 1);
+    ms.abort = 0;
+    ms.range_err = 0;
+    ptx::fence_mbar_init();
+  }
+  if (threadIdx.x < kHeads) ms.m_ref[threadIdx.x] = -CUDART_INF_F;
+  if (warp == 0) {
+    ptx::tmem_alloc(&ms.tmem_slot, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  x.tmem = ms.tmem_slot;
+
+  if (warp >= kSoftWarps) gather_role(x, warp, lane);
+  else softmax_role(x, warp, lane);
+
+  // ------------------------------------------------------------------ epilogue
+  bool ok = ptx::mbar_wait_warp(&ms.pv_done, (x.n_tiles - 1) & 1, x.abort, lane);
+  ptx::tc_fence_after();
+  __syncthreads();                           // row sums of the softmax warps are in ms.red
+  if (threadIdx.x < kHeads) {
+    const int h = threadIdx.x;
+    const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
+    ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
+    ms.lse_out[h] = L > 0.f ? (ms.m_ref[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
+  }
+  __syncthreads();
+  epilogue(x, warp, lane, ok && !ms.abort);
+  if ((int)threadIdx.x < x.hg_valid) {
+    const size_t h = (size_t)x.g * kHeads + threadIdx.x;
+    if (p.final_out) p.lse[(size_t)x.b * p.H + h] = ms.lse_out[threadIdx.x];
+    else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = ms.lse_out[threadIdx.x];
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (threadIdx.x == 0) {
+    // every MMA has completed before TMEM is released (time limit only)
+    volatile int no_abort = 0;
+    const bool drained = ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
+    if (p.err) {
+      if (ms.abort || !drained) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+      if (ms.range_err) atomicOr(p.err, SMLA_DEVERR_RANGE);
+    }
+  }
+  __syncthreads();
+  if (warp == 0) ptx::tmem_dealloc(x.tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool split_shape_supported(int H, int topk) {
+  return (H == 16 || H == 32 || H == 64 || H == 128) && topk >= 1 && topk <= kMaxTopk;
+}
+
+int split_heads_per_cta() { return kHeads; }
+
+int split_ctas_per_unit() { return 1; }
+
+int split_ctas_per_sm(int H) {
+  (void)H;
+  return 1;
+}
+
+cudaError_t launch_split(const SplitParams& p, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  const int head_groups = (p.H + kHeads - 1) / kHeads;
+  dim3 grid(p.nsplit, head_groups, p.B);
+  split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace smla

