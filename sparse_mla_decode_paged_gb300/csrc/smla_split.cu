@@ -44,7 +44,8 @@
 //                      QK, resp. the PV of block 0) and thread 0 issues that
 //                      block's 8 MMAs, so writing P * mant_{b+1} overlaps PV
 //                      of block b.
-//   epilogue (all)     O / l from TMEM straight to global memory, lse.
+//   epilogue (all)     O / l from TMEM written straight to the [head][512] output
+//                      rows (two dims per lane and store), lse.
 //
 // Shared memory: Q 72 KB + K tile 144 KB + ~4 KB; TMEM: O^T in columns
 // 0..255 (4 blocks x 64 heads), score buffers in 256..511.
@@ -84,10 +85,10 @@ constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
 struct Misc {
   uint64_t q_ready;          // Q staged (one arrival per softmax warp)
   uint64_t tile_full;        // K tile and metadata of the tile written (one arrival per gather warp)
-  uint64_t s_full[4];        // score buffer b holds block b of the tile
+  uint64_t s_full[2];        // score buffer b holds block b of the tile (b = 0, 1)
   uint64_t s_free0;          // buffer 0 read out (one arrival per softmax warp): the rope may go there
-  uint64_t r_full;           // buffer 0 holds the rope scores
-  uint64_t pv0_done, pv1_done;
+  uint64_t r_full;           // buffer 0 holds the rope scores, buffers 2 and 3 blocks 2 and 3
+  uint64_t pv0_done;          // PV of block 0 complete: chunks 0, 1 and the rope chunk are free
   uint64_t pv_done;          // every PV MMA of the tile complete: the K tile is free
   uint64_t teardown;         // every MMA complete
   uint32_t tmem_slot;
@@ -108,6 +109,32 @@ static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
   return row * 128u + ((unit ^ (row & 7u)) << 4);
+}
+
+// MMA issue.  A descriptor's start address sits in its low 14 bits in 16-byte units, so the operand
+// at byte offset o from a base is the base descriptor + o / 16 (shared addresses stay below 256 KB:
+// no carry).  The issuers are unrolled with compile-time offsets: one thread issues every MMA, and
+// rebuilding each descriptor on that thread costs more than the MMA itself.
+//
+// QK of chunks [ch0, ch0 + nch) into one score buffer.
+template <int kCh0, int kNch>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dK, uint64_t dQ) {
+#pragma unroll
+  for (int cc = 0; cc < kNch; ++cc)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      ptx::mma_f16_ss(d_tmem, dK + (uint64_t)(((kCh0 + cc) * kKChunk + 32 * kk) >> 4),
+                      dQ + (uint64_t)(((kCh0 + cc) * kQChunk + 32 * kk) >> 4), kIdescQK, (cc | kk) != 0);
+}
+
+// PV of latent block kB: O^T_b (+)= K'_b^T . (P * mant_b); A is the K tile read MN-major (dims of
+// chunks 2b, 2b + 1), B the 16-token slices of the P * mant buffer.
+template <int kB>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t dV, uint64_t dBuf, bool accumulate) {
+#pragma unroll
+  for (int kk = 0; kk < kTile / 16; ++kk)
+    ptx::mma_f16_ss(tmem + 64 * kB, dV + (uint64_t)((2 * kB * kKChunk + kk * 2048) >> 4),
+                    dBuf + (uint64_t)((kk * 2048) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -237,13 +264,23 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     sc = off_own >= 0 ? ptx::ldg_stream(kv + off_own + 512) : make_uint4(0, 0, 0, 0);
   };
 
-  // prologue: tile 0 resolved and its records in flight; tile 1's page and tile 2's entries in flight
+  // Records of tile i + 2 are prefetched into L2 when tile i's are loaded into registers, so the
+  // register loads (which L1 can hold only ~28 KB of) see L2 latency.
+  auto prefetch_row = [&](int64_t r) {
+    if (lane < 16 && r >= 0) ptx::prefetch_l2_bulk(kv + r * kRecordBytes, kRecordBytes);
+  };
+  // prologue: tile 0 resolved and its records in flight, tiles 1 and 2 prefetched; tile 3's page and
+  // tile 4's entries in flight
   const int t0 = topk_load(0);
-  int t1 = topk_load(1);
-  int64_t row = row_from(t0, page_load(t0));
+  int t1 = topk_load(1), t2 = topk_load(2), t3 = topk_load(3);
+  const int pg0 = page_load(t0);
+  int pg1 = page_load(t1), pg2 = page_load(t2);
+  int64_t row = row_from(t0, pg0);
   load_tile(row);
-  int pg1 = page_load(t1);
-  int t2 = topk_load(2);
+  if (x.n_tiles > 1) prefetch_row(row_from(t1, pg1));
+  if (x.n_tiles > 2) prefetch_row(row_from(t2, pg2));
+  int pg3 = page_load(t3);
+  int t4 = topk_load(4);
 
   for (int i = 0; i < x.n_tiles; ++i) {
     const bool valid = row >= 0;
@@ -293,12 +330,15 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     ptx::fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(&ms.tile_full);
-    // tile i + 1's records, tile i + 2's pages, tile i + 3's entries
+    // tile i + 1's records, tile i + 3's into L2, tile i + 4's pages, tile i + 5's entries
     row = row_from(t1, pg1);
     if (i + 1 < x.n_tiles) load_tile(row);
-    pg1 = page_load(t2);
-    t1 = t2;
-    t2 = topk_load(i + 3);
+    if (i + 3 < x.n_tiles) prefetch_row(row_from(t3, pg3));
+    t1 = t2; pg1 = pg2;
+    t2 = t3; pg2 = pg3;
+    t3 = t4;
+    pg3 = page_load(t4);
+    t4 = topk_load(i + 5);
   }
   if (range_bad) ms.range_err = 1;
 }
@@ -308,7 +348,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   const SplitParams& p = *x.p;
   Misc& ms = *x.ms;
   const int t = threadIdx.x;                 // token of the tile = TMEM lane
-  const bool issuer = (t == 0);              // every MMA
+  const bool issue_warp = (warp == 0);       // one elected lane of warp 0 issues every MMA
   const uint32_t lane_q = (uint32_t)(32 * warp) << 16;
   int range_bad = 0;
   bool ok = true, mma_ok = true;
@@ -338,30 +378,30 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 
   const float c2 = p.sm_scale * 1.4426950408889634f;
   float lsum0 = 0.f, lsum1 = 0.f;            // this warp's row sums of heads 2 lane, 2 lane + 1
-  const uint32_t bufR = x.k_base + kRopeChunk * kKChunk, buf0 = x.k_base;
+  const uint32_t bufR = x.k_base + kRopeChunk * kKChunk, buf0 = x.k_base, buf1 = x.k_base + kKChunk;
+  const uint64_t dK = ptx::sw128_desc(x.k_base, 16, 1024), dQ = ptx::sw128_desc(x.q_base, 16, 1024);
+  const uint64_t dV = ptx::sw128_desc(x.k_base, kKChunk, 1024);   // K tile as the MN-major A of PV
+  // P * mant buffers as MN-major B: one 64-head atom along N, so the leading offset is never stepped
+  const uint64_t dBufR = ptx::sw128_desc(bufR, 1024, 1024), dBuf0 = ptx::sw128_desc(buf0, 1024, 1024),
+                 dBuf1 = ptx::sw128_desc(buf1, 1024, 1024);
 
   for (int i = 0; i < x.n_tiles; ++i) {
     const uint32_t ph = i & 1;
     ok = ptx::mbar_wait_warp(&ms.tile_full, ph, x.abort, lane) && ok;
-    if (issuer) {
-      // QK of the four latent blocks, block b into score buffer b
-      if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_bounded(&ms.q_ready, 0, x.abort);
+    // QK of latent block b into score buffer b; blocks 0 and 1 first, the rest (and the rope, into
+    // buffer 0) once block 0 has been read out, so that warp 0 reads block 0 while block 1 runs
+    if (issue_warp) {
+      if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane);
       mma_ok = mma_ok && ok;
       if (mma_ok) {
         ptx::tc_fence_after();
-#pragma unroll 1
-        for (int bb = 0; bb < 4; ++bb) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int ch = 2 * bb + cc;
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::mma_f16_ss(x.tmem + kSCol + 64 * bb, ptx::sw128_desc(x.k_base + ch * kKChunk + 32 * kk, 16, 1024),
-                              ptx::sw128_desc(x.q_base + ch * kQChunk + 32 * kk, 16, 1024), kIdescQK,
-                              (cc | kk) != 0);
-          }
-          ptx::mma_commit(&ms.s_full[bb]);
+        if (ptx::elect_one()) {
+          issue_qk<0, 2>(x.tmem + kSCol, dK, dQ);
+          ptx::mma_commit(&ms.s_full[0]);
+          issue_qk<2, 2>(x.tmem + kSCol + 64, dK, dQ);
+          ptx::mma_commit(&ms.s_full[1]);
         }
+        __syncwarp();
       }
     }
     __syncwarp();
@@ -372,10 +412,12 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     float s[64];
 #pragma unroll
     for (int h = 0; h < 64; ++h) s[h] = 0.f;
-    // scores: block buffers as they complete, then the rope
+    // scores, buffers in the order they complete: block 0, block 1, then the rope (buffer 0), block 2
+    // and block 3 (one commit for the three)
 #pragma unroll 1
-    for (int bb = 0; bb < 5; ++bb) {
-      ok = ptx::mbar_wait_warp(bb < 4 ? &ms.s_full[bb] : &ms.r_full, ph, x.abort, lane) && ok;
+    for (int k = 0; k < 5; ++k) {
+      const int bb = k < 2 ? k : k == 2 ? 4 : k - 1;      // 4 = rope
+      if (k < 3) ok = ptx::mbar_wait_warp(k < 2 ? &ms.s_full[k] : &ms.r_full, ph, x.abort, lane) && ok;
       if (ok) {
         ptx::tc_fence_after();
         const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : bb == 3 ? mant[3] : 1.f);
@@ -389,25 +431,24 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
           for (int h = 0; h < 32; ++h) s[32 * hh + h] = fmaf(f, __uint_as_float(r[h]), s[32 * hh + h]);
         }
       }
-      if (bb == 0) {
+      if (k == 0) {
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ms.s_free0);
-        if (issuer) {
-          // the rope scores go to buffer 0 once every warp has read block 0 out of it
-          mma_ok = mma_ok && ptx::mbar_wait_bounded(&ms.s_free0, ph, x.abort);
+        if (issue_warp) {
+          // buffer 0 is free once every warp has read block 0 out of it
+          mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.s_free0, ph, x.abort, lane);
           if (mma_ok) {
             ptx::tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              ptx::mma_f16_ss(x.tmem + kSCol,
-                              ptx::sw128_desc(x.k_base + kRopeChunk * kKChunk + 32 * kk, 16, 1024),
-                              ptx::sw128_desc(x.q_base + kRopeChunk * kQChunk + 32 * kk, 16, 1024), kIdescQK,
-                              kk != 0);
-            ptx::mma_commit(&ms.r_full);
+            if (ptx::elect_one()) {
+              issue_qk<kRopeChunk, 1>(x.tmem + kSCol, dK, dQ);
+              issue_qk<4, 2>(x.tmem + kSCol + 128, dK, dQ);
+              issue_qk<6, 2>(x.tmem + kSCol + 192, dK, dQ);
+              ptx::mma_commit(&ms.r_full);
+            }
+            __syncwarp();
           }
         }
-        __syncwarp();
       }
     }
 #pragma unroll
@@ -475,9 +516,6 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       ph2[2 * k] = f32x2_to_f16x2_sat(s[4 * k], s[4 * k + 1]);
       ph2[2 * k + 1] = f32x2_to_f16x2_sat(s[4 * k + 2], s[4 * k + 3]);
     }
-    const float2 ps = reduce_scatter64<false>(s, lane);
-    lsum0 += ps.x;
-    lsum1 += ps.y;
 
     // PV block by block: P * mant_b into the rope chunk (b = 0, 2) or chunk 0 (b = 1, 3), each free
     // once the MMAs reading it are done (the rope QK, resp. the PV of block 0)
@@ -489,79 +527,97 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
         ptx::sts128_async_only(buf + swz128(t, u), make_uint4(hmul2(ph2[4 * u], m2), hmul2(ph2[4 * u + 1], m2),
                                                               hmul2(ph2[4 * u + 2], m2), hmul2(ph2[4 * u + 3], m2)));
     };
-    auto issue_pv = [&](int bb, uint32_t buf) {
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk)
-        ptx::mma_f16_ss(x.tmem + 64 * bb, ptx::sw128_desc(x.k_base + 2 * bb * kKChunk + kk * 2048, kKChunk, 1024),
-                        // P spans one 64-head atom along N: its leading offset is never stepped
-                        ptx::sw128_desc(buf + kk * 2048, 1024, 1024), kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
-    };
     write_pm(0, bufR);
     ptx::fence_proxy_async_smem();
     ptx::tc_fence_before();
     ptx::named_bar_sync(2, kSoftThreads);
-    if (issuer) {
+    if (issue_warp) {
       mma_ok = mma_ok && ok;
       if (mma_ok) {
         ptx::tc_fence_after();
-        issue_pv(0, bufR);
-        ptx::mma_commit(&ms.pv0_done);
+        if (ptx::elect_one()) {
+          issue_pv<0>(x.tmem, dV, dBufR, i > 0);
+          ptx::mma_commit(&ms.pv0_done);
+        }
+        __syncwarp();
       }
     }
+    // row sums, while block 0's PV runs
+    {
+      const float2 ps = reduce_scatter64<false>(s, lane);
+      lsum0 += ps.x;
+      lsum1 += ps.y;
+    }
     ok = ptx::mbar_wait_warp(&ms.pv0_done, ph, x.abort, lane) && ok;
+    // block 0's PV is done: chunks 0 and 1 and the rope chunk take P * mant of blocks 1..3
     write_pm(1, buf0);
     write_pm(2, bufR);
+    write_pm(3, buf1);
     ptx::fence_proxy_async_smem();
     ptx::named_bar_sync(2, kSoftThreads);
-    if (issuer && mma_ok) {
+    if (issue_warp && mma_ok) {
       ptx::tc_fence_after();
-      issue_pv(1, buf0);
-      ptx::mma_commit(&ms.pv1_done);
-      issue_pv(2, bufR);
-    }
-    ok = ptx::mbar_wait_warp(&ms.pv1_done, ph, x.abort, lane) && ok;
-    write_pm(3, buf0);
-    ptx::fence_proxy_async_smem();
-    ptx::named_bar_sync(2, kSoftThreads);
-    if (issuer && mma_ok) {
-      ptx::tc_fence_after();
-      issue_pv(3, buf0);
-      ptx::mma_commit(&ms.pv_done);
+      if (ptx::elect_one()) {
+        issue_pv<1>(x.tmem, dV, dBuf0, i > 0);
+        issue_pv<2>(x.tmem, dV, dBufR, i > 0);
+        issue_pv<3>(x.tmem, dV, dBuf1, i > 0);
+        ptx::mma_commit(&ms.pv_done);
+      }
+      __syncwarp();
     }
   }
   if (range_bad) ms.range_err = 1;
-  if (issuer) ptx::mma_commit(&ms.teardown);
+  if (issue_warp) {
+    if (ptx::elect_one()) ptx::mma_commit(&ms.teardown);
+    __syncwarp();
+  }
   ms.red[warp][2 * lane] = lsum0;
   ms.red[warp][2 * lane + 1] = lsum1;
 }
 
 // ------------------------------------------------------------------------------------------ epilogue
-// All 12 warps: warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and
-// the 32-column chunks c = w / 4, w / 4 + 3, ... of O^T (chunk c: block c / 2, heads 32 (c % 2) ..).
-__device__ __forceinline__ void epilogue(const Ctx& x, int warp, int lane, bool ok) {
+// All 12 warps write O / l from TMEM straight to the output rows [head][512] (bf16, or fp32
+// partials): warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and the
+// 32-column chunks c = w / 4, w / 4 + 3, ... of O^T (chunk c: block c / 2, heads 32 (c % 2) ..).
+// Lanes 2j, 2j + 1 hold dims d, d + 1; for heads h, h + 1 the even lane writes row h and the odd lane
+// row h + 1, two dims each, so a warp store covers two 64- (bf16) or 128-byte (fp32) row segments.
+__device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane) {
   const SplitParams& p = *x.p;
   Misc& ms = *x.ms;
-  if (!ok) return;
   const int quad = warp & 3;
   const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
+  const bool odd = lane & 1;
+  const size_t head0 = (size_t)x.g * kHeads;
+#pragma unroll 1
   for (int c = warp >> 2; c < 8; c += 3) {
     const int jb = c >> 1, hb = 32 * (c & 1);
     uint32_t r[32];
     ptx::tmem_ld32(x.tmem + lane_q + 32 * c, r);
+    float v[32];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 l4 = reinterpret_cast<const float4*>(ms.linv + hb)[k];
+      v[4 * k] = l4.x; v[4 * k + 1] = l4.y; v[4 * k + 2] = l4.z; v[4 * k + 3] = l4.w;
+    }
     ptx::tmem_wait_ld();
-    const int d = 128 * jb + 32 * quad + lane;
-    const size_t hrow0 = (size_t)x.g * kHeads + hb;
-    if (p.final_out) {
-      uint16_t* o = p.out + ((size_t)x.b * p.H + hrow0) * kDLatent + d;
 #pragma unroll
-      for (int h = 0; h < 32; ++h)
-        if (hb + h < x.hg_valid)
-          o[(size_t)h * kDLatent] = (uint16_t)(f32x2_to_bf16x2(__uint_as_float(r[h]) * ms.linv[hb + h], 0.f) & 0xFFFFu);
-    } else {
-      float* o = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + hrow0) * kDLatent + d;
+    for (int h = 0; h < 32; ++h) v[h] *= __uint_as_float(r[h]);
+    const int d0 = 128 * jb + 32 * quad + (lane & ~1);
 #pragma unroll
-      for (int h = 0; h < 32; ++h)
-        if (hb + h < x.hg_valid) o[(size_t)h * kDLatent] = __uint_as_float(r[h]) * ms.linv[hb + h];
+    for (int h = 0; h < 32; h += 2) {
+      const float mine = odd ? v[h + 1] : v[h];
+      const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
+      const float lo = odd ? other : mine, hi = odd ? mine : other;   // dims d0, d0 + 1
+      const int hl = hb + h + (odd ? 1 : 0);
+      if (hl < x.hg_valid) {
+        if (p.final_out) {
+          uint16_t* dst = p.out + ((size_t)x.b * p.H + head0 + hl) * kDLatent + d0;
+          *reinterpret_cast<uint32_t*>(dst) = f32x2_to_bf16x2(lo, hi);
+        } else {
+          float* dst = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + head0 + hl) * kDLatent + d0;
+          *reinterpret_cast<float2*>(dst) = make_float2(lo, hi);
+        }
+      }
     }
   }
 }
@@ -605,11 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   if (threadIdx.x == 0) {
     ptx::mbar_init(&ms.q_ready, kSoftWarps);
     ptx::mbar_init(&ms.tile_full, kGatherWarps);
-    for (int bb = 0; bb < 4; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
+    for (int bb = 0; bb < 2; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
     ptx::mbar_init(&ms.s_free0, kSoftWarps);
     ptx::mbar_init(&ms.r_full, 1);
     ptx::mbar_init(&ms.pv0_done, 1);
-    ptx::mbar_init(&ms.pv1_done, 1);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
     ms.abort = 0;
@@ -640,11 +695,15 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     ms.lse_out[h] = L > 0.f ? (ms.m_ref[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
   }
   __syncthreads();
-  epilogue(x, warp, lane, ok && !ms.abort);
-  if ((int)threadIdx.x < x.hg_valid) {
-    const size_t h = (size_t)x.g * kHeads + threadIdx.x;
-    if (p.final_out) p.lse[(size_t)x.b * p.H + h] = ms.lse_out[threadIdx.x];
-    else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = ms.lse_out[threadIdx.x];
+  const bool out_ok = ok && !ms.abort;
+  if (out_ok) {
+    epilogue_write(x, warp, lane);
+    if ((int)threadIdx.x < x.hg_valid) {
+      const int hl = threadIdx.x;
+      const size_t h = (size_t)x.g * kHeads + hl;
+      if (p.final_out) p.lse[(size_t)x.b * p.H + h] = ms.lse_out[hl];
+      else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = ms.lse_out[hl];
+    }
   }
 
   ptx::tc_fence_before();
