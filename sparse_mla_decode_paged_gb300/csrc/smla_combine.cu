@@ -4,6 +4,7 @@
 #include <math_constants.h>
 
 #include "smla_device.cuh"
+#include "smla_ptx.cuh"
 
 namespace smla {
 namespace {
@@ -22,6 +23,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsp
   const int tid = threadIdx.x;
   __shared__ float w_s[kMaxCombineSplit];
   __shared__ float lse_s;
+  // launched as a programmatic dependent of the split kernel: its partials are complete and visible
+  // only after this wait (a no-op for an ordinary launch)
+  ptx::griddep_wait();
   if (tid < 32) {
     float m = -CUDART_INF_F;
     for (int s = tid; s < nsplit; s += 32) m = fmaxf(m, __ldg(lse_part + ((size_t)b * nsplit + s) * H + h));
@@ -74,8 +78,19 @@ __global__ void gather_rows_kernel(const int32_t* __restrict__ bt, const int32_t
 
 cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part, uint16_t* out,
                            float* lse, cudaStream_t stream) {
-  combine_kernel<<<B * H, kCombineThreads, 0, stream>>>(H, nsplit, o_part, lse_part, out, lse);
-  return cudaGetLastError();
+  // programmatic stream serialization: the merge's CTAs may be scheduled while the split kernel
+  // (which signals at its start) still runs; each waits for the split grid in griddep_wait
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(B * H);
+  cfg.blockDim = dim3(kCombineThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, H, nsplit, o_part, lse_part, out, lse);
 }
 
 cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens, int B, int topk_n,

@@ -311,6 +311,19 @@ __device__ __forceinline__ int ldg_i32_now(const int32_t* p) {
 
 // Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 (TMA engine; no
 // registers or L1 space are used and nothing waits for it).
+// Programmatic dependent launch: a grid launched with programmatic stream serialization after this
+// one may start once every CTA here has signalled (or exited); it waits for this grid's completion
+// and memory with griddep_wait before touching its results.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// The 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2_line(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }

@@ -15,16 +15,17 @@
 
 namespace smla {
 
-// Cost-model constants (microseconds) of the split kernel on GB300: a fixed
-// per-CTA latency (launch, index chain, first loads, tail), a per-token cost
-// for one 64-head group, the per-CTA cost of writing fp32 partials, and the
-// merge kernel.
+// Cost-model constants (microseconds) of the split kernel on GB300, fitted to its measured times: a
+// fixed per-CTA latency (launch, index chain, Q and first record loads, epilogue), a per-tile cost with
+// a part that scales with the top-k entries of the tile (record loads and conversion), the extra cost
+// of fp32 partial rows over the bf16 output, and the merge kernel.
 struct CostModel {
-  double cta_fixed_us = 8.0;         // launch, index chain, Q load, first loads, epilogue
-  double per_tile_us = 16.0;         // one tile of 128 top-k entries for a 64-head group
-  double per_token_us = 0.03;        // partial tiles cost less
-  double combine_fixed_us = 2.0;
-  double combine_gbs = 3000.0;       // partial bytes read + out written
+  double cta_fixed_us = 13.0;
+  double tile_fixed_us = 3.3;
+  double tile_token_us = 3.0 / 128;
+  double partial_extra_us = 0.7;       // 128 KB of fp32 partial rows instead of 64 KB of bf16 output
+  double combine_fixed_us = 2.0;       // merge kernel: launch (overlapped with the split kernel's tail)
+  double combine_gbs = 6000.0;
 };
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -62,9 +63,9 @@ static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit
   const double waves = ctas / slots;
   const int whole_waves = (int)ceil(waves - 1e-9);
   const int tokens = split_len < topk ? split_len : topk;
-  const int tiles = (tokens + 127) / 128;
-  const double cta_us = m.cta_fixed_us + m.per_tile_us * (tiles - 1) + m.per_token_us * (tokens - 128 * (tiles - 1)) +
-                        (m.per_tile_us - 128 * m.per_token_us);
+  double cta_us = m.cta_fixed_us;
+  for (int left = tokens; left > 0; left -= 128) cta_us += m.tile_fixed_us + m.tile_token_us * (left < 128 ? left : 128);
+  if (nsplit > 1) cta_us += m.partial_extra_us;
   double t = whole_waves * cta_us;
   if (nsplit > 1) {
     const double bytes = (double)B * H * (nsplit * (kDLatent * 4.0 + 4.0) + kDLatent * 2.0 + 4.0);

@@ -225,6 +225,14 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   int range_bad = 0;
   bool ok = true;
 
+  // the block-table row of the query into L2 (one 128-byte line per gather lane, up to 32 KB), so the
+  // page lookups after the top-k loads see L2 latency
+  {
+    const int pages = min(p.max_pages, (seq_len + kPageSize - 1) / kPageSize);
+    const int line = 32 * gw + lane;
+    if (line * 32 < pages) ptx::prefetch_l2_line(bt_row + line * 32);
+  }
+
   // Index -> row (a1) in three stages.  A top-k entry t is used when 0 <= t < seq_len; its
   // logical page t / 64 must lie in the block-table row and the physical page in the cache, else
   // the entry is skipped and flagged.
@@ -276,6 +284,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   const int pg0 = page_load(t0);
   int pg1 = page_load(t1), pg2 = page_load(t2);
   int64_t row = row_from(t0, pg0);
+  prefetch_row(row);                         // the register loads below get ~28 KB of L1: the rest hit L2
   load_tile(row);
   if (x.n_tiles > 1) prefetch_row(row_from(t1, pg1));
   if (x.n_tiles > 2) prefetch_row(row_from(t2, pg2));
@@ -388,6 +397,10 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   for (int i = 0; i < x.n_tiles; ++i) {
     const uint32_t ph = i & 1;
     ok = ptx::mbar_wait_warp(&ms.tile_full, ph, x.abort, lane) && ok;
+    const bool valid = ms.valid[t];
+    float mant[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) mant[q] = ms.mant[q][t];
     // QK of latent block b into score buffer b; blocks 0 and 1 first, the rest (and the rope, into
     // buffer 0) once block 0 has been read out, so that warp 0 reads block 0 while block 1 runs
     if (issue_warp) {
@@ -405,10 +418,6 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       }
     }
     __syncwarp();
-    const bool valid = ms.valid[t];
-    float mant[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) mant[q] = ms.mant[q][t];
     float s[64];
 #pragma unroll
     for (int h = 0; h < 64; ++h) s[h] = 0.f;
@@ -422,13 +431,14 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
         ptx::tc_fence_after();
         const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : bb == 3 ? mant[3] : 1.f);
         const uint32_t sa = x.tmem + lane_q + kSCol + 64 * (bb < 4 ? bb : 0);
+        uint32_t r0[32], r1[32];
+        ptx::tmem_ld32(sa, r0);
+        ptx::tmem_ld32(sa + 32, r1);
+        ptx::tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t r[32];
-          ptx::tmem_ld32(sa + 32 * hh, r);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int h = 0; h < 32; ++h) s[32 * hh + h] = fmaf(f, __uint_as_float(r[h]), s[32 * hh + h]);
+        for (int h = 0; h < 32; ++h) {
+          s[h] = fmaf(f, __uint_as_float(r0[h]), s[h]);
+          s[32 + h] = fmaf(f, __uint_as_float(r1[h]), s[32 + h]);
         }
       }
       if (k == 0) {
@@ -627,6 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(base + kMiscOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the merge (launched as a programmatic dependent) may be scheduled now: it waits for this grid
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
 
   Ctx x;
   x.p = &p;

@@ -46,6 +46,15 @@ def test_every_split_count(nsplit):
     compare(out, lse, *oracle_on(w))
 
 
+@pytest.mark.parametrize("H,nsplit", [(16, 4), (32, 8), (64, 5), (128, 3), (64, 2)])
+def test_split_merge_heads_and_partitions(H, nsplit):
+    # head counts of one or two groups, partitions made only of padding (ctx 40 < topk), several
+    # tiles per partition, partition counts that do not divide the top-k list
+    w = _custom(B=4, H=H, topk=448, ctx=[3000, 40, 448, 1200], seed=40 + nsplit, outlier_channels=3)
+    out, lse = _run(w, nsplit=nsplit)
+    compare(out, lse, *oracle_on(w))
+
+
 def test_split_and_combine_entry_points():
     w = _custom(B=2, H=64, topk=200, ctx=[900, 150], seed=32)
     o_part, lse_part = api.sparse_mla_split(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale, 3)
