@@ -12,7 +12,11 @@ namespace {
 constexpr int kCombineThreads = 128;   // 4 output dims per thread
 
 // One CTA per (query, head): lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) o_s.
-// "The 64-Block Barrier", "The Split-K Prescription" (online-softmax merge).
+// "The 64-Block Barrier", "The Split-K Prescription" (online-softmax merge).  Each thread puts its
+// partial-row loads (up to kBatch partitions) in flight before the weights are known, so a call costs
+// one round trip to the partials rather than two.
+constexpr int kBatch = 8;
+
 __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsplit,
                                                                   const float* __restrict__ o_part,
                                                                   const float* __restrict__ lse_part,
@@ -26,6 +30,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsp
   // launched as a programmatic dependent of the split kernel: its partials are complete and visible
   // only after this wait (a no-op for an ordinary launch)
   ptx::griddep_wait();
+  const float4* rows = reinterpret_cast<const float4*>(o_part + ((size_t)b * nsplit * H + h) * kDLatent) + tid;
+  const size_t split_stride = (size_t)H * kDLatent / 4;      // float4s between partitions of a row
+  float4 v[kBatch];
+#pragma unroll
+  for (int s = 0; s < kBatch; ++s) v[s] = s < nsplit ? __ldg(rows + s * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
   if (tid < 32) {
     float m = -CUDART_INF_F;
     for (int s = tid; s < nsplit; s += 32) m = fmaxf(m, __ldg(lse_part + ((size_t)b * nsplit + s) * H + h));
@@ -47,14 +56,22 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsp
   }
   __syncthreads();
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < nsplit; ++s) {
-    const float w = w_s[s];
-    if (w == 0.f) continue;
-    const float4 v = __ldg(reinterpret_cast<const float4*>(o_part + (((size_t)b * nsplit + s) * H + h) * kDLatent) + tid);
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  for (int s0 = 0; s0 < nsplit; s0 += kBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int s = 0; s < kBatch; ++s)
+        v[s] = s0 + s < nsplit ? __ldg(rows + (s0 + s) * split_stride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int s = 0; s < kBatch; ++s) {
+      if (s0 + s >= nsplit) break;
+      const float w = w_s[s0 + s];
+      if (w == 0.f) continue;          // a partition with no entry: its row is not read into the sum
+      acc.x = fmaf(w, v[s].x, acc.x);
+      acc.y = fmaf(w, v[s].y, acc.y);
+      acc.z = fmaf(w, v[s].z, acc.z);
+      acc.w = fmaf(w, v[s].w, acc.w);
+    }
   }
   uint2 packed;
   packed.x = f32x2_to_bf16x2(acc.x, acc.y);

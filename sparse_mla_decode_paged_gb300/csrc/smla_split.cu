@@ -85,9 +85,7 @@ constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
 struct Misc {
   uint64_t q_ready;          // Q staged (one arrival per softmax warp)
   uint64_t tile_full;        // K tile and metadata of the tile written (one arrival per gather warp)
-  uint64_t s_full[2];        // score buffer b holds block b of the tile (b = 0, 1)
-  uint64_t s_free0;          // buffer 0 read out (one arrival per softmax warp): the rope may go there
-  uint64_t r_full;           // buffer 0 holds the rope scores, buffers 2 and 3 blocks 2 and 3
+  uint64_t s_full[4];        // score buffer b holds block b of the tile (block 0 with the rope)
   uint64_t pv0_done;          // PV of block 0 complete: chunks 0, 1 and the rope chunk are free
   uint64_t pv_done;          // every PV MMA of the tile complete: the K tile is free
   uint64_t teardown;         // every MMA complete
@@ -117,14 +115,15 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
 // rebuilding each descriptor on that thread costs more than the MMA itself.
 //
 // QK of chunks [ch0, ch0 + nch) into one score buffer.
-template <int kCh0, int kNch>
+template <int kCh0, int kNch, bool kAccumulate = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dK, uint64_t dQ) {
 #pragma unroll
   for (int cc = 0; cc < kNch; ++cc)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       ptx::mma_f16_ss(d_tmem, dK + (uint64_t)(((kCh0 + cc) * kKChunk + 32 * kk) >> 4),
-                      dQ + (uint64_t)(((kCh0 + cc) * kQChunk + 32 * kk) >> 4), kIdescQK, (cc | kk) != 0);
+                      dQ + (uint64_t)(((kCh0 + cc) * kQChunk + 32 * kk) >> 4), kIdescQK,
+                      (kAccumulate || cc != 0 || kk != 0) ? 1u : 0u);
 }
 
 // PV of latent block kB: O^T_b (+)= K'_b^T . (P * mant_b); A is the K tile read MN-major (dims of
@@ -153,6 +152,23 @@ __device__ __forceinline__ float pow2_split(float sc, uint32_t& p2) {
   return mant;
 }
 
+// Block 0's scale, split so that mant >= 1 always (the rope is folded into block 0 as rope / mant):
+// e = clamp(exponent(sc), -30, 7); 2^e as fp16 bits (subnormal below 2^-14, zero below 2^-24, where
+// K' = code * 2^e is rounded or vanishes: such a block contributes below 2^-15 * 448 * |q|); sc == 0
+// gives mant = 1 and 2^e = 0.
+__device__ __forceinline__ float pow2_split_b0(float sc, uint32_t& p2) {
+  const uint32_t bits = __float_as_uint(sc) & 0x7fffffffu;
+  if (bits < 0x00800000u) {                  // zero or fp32-subnormal scale: the block contributes nothing
+    p2 = 0;
+    return 1.f;
+  }
+  int e = (int)(bits >> 23) - 127;
+  e = max(-30, min(7, e));
+  const float mant = sc * __uint_as_float((uint32_t)(127 - e) << 23);
+  p2 = e >= -14 ? (uint32_t)(e + 15) << 10 : e >= -24 ? (1u << (e + 24)) : 0u;
+  return mant;
+}
+
 // 2 bf16 -> 2 fp16 (saturating); flags values outside the fp16 range.
 __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, int& range_bad) {
   const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
@@ -163,6 +179,18 @@ __device__ __forceinline__ uint32_t bf2_to_h2(uint32_t w, int& range_bad) {
 __device__ __forceinline__ uint4 bf8_to_h8(uint4 v, int& range_bad) {
   return make_uint4(bf2_to_h2(v.x, range_bad), bf2_to_h2(v.y, range_bad), bf2_to_h2(v.z, range_bad),
                     bf2_to_h2(v.w, range_bad));
+}
+
+// 2 bf16 times `f` (fp32) -> 2 fp16, rounded once (saturating; flags values outside the fp16 range).
+__device__ __forceinline__ uint32_t bf2_scaled_to_h2(uint32_t w, float f, int& range_bad) {
+  const float lo = __uint_as_float(w << 16) * f, hi = __uint_as_float(w & 0xFFFF0000u) * f;
+  range_bad |= (fabsf(lo) > kFp16Max) | (fabsf(hi) > kFp16Max);
+  return f32x2_to_f16x2_sat(lo, hi);
+}
+
+__device__ __forceinline__ uint4 bf8_scaled_to_h8(uint4 v, float f, int& range_bad) {
+  return make_uint4(bf2_scaled_to_h2(v.x, f, range_bad), bf2_scaled_to_h2(v.y, f, range_bad),
+                    bf2_scaled_to_h2(v.z, f, range_bad), bf2_scaled_to_h2(v.w, f, range_bad));
 }
 
 __device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
@@ -299,9 +327,11 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
       const float s4[4] = {__uint_as_float(sc.x), __uint_as_float(sc.y), __uint_as_float(sc.z),
                            __uint_as_float(sc.w)};
       uint32_t e[4];
+      float inv_m0 = 0.f;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const float mt = pow2_split(s4[q], e[q]);
+        const float mt = q == 0 ? pow2_split_b0(s4[0], e[0]) : pow2_split(s4[q], e[q]);
+        if (q == 0) inv_m0 = __frcp_rn(mt);
         if (lane < 16) ms.mant[q][tl] = valid ? mt : 0.f;
         if (valid) range_bad |= !(fabsf(s4[q]) <= kMaxScale);
       }
@@ -328,10 +358,14 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
         ptx::sts128_async_only(cb + swz128(t, u0 + sw), sw ? hi4 : lo4);
         ptx::sts128_async_only(cb + swz128(t, u0 + 1 - sw), sw ? lo4 : hi4);
       }
+      // the rope, divided by the token's block-0 mantissa: its MMAs accumulate into block 0's scores,
+      // which the softmax scales by mant_0
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t t = kTokPerGatherWarp * gw + 4 * k + (lane >> 3);
-        ptx::sts128_async_only(x.k_base + kRopeChunk * kKChunk + swz128(t, lane & 7), bf8_to_h8(rope[k], range_bad));
+        const float f = __shfl_sync(0xffffffffu, inv_m0, 4 * k + (lane >> 3));
+        ptx::sts128_async_only(x.k_base + kRopeChunk * kKChunk + swz128(t, lane & 7),
+                               bf8_scaled_to_h8(rope[k], f, range_bad));
       }
     }
     // the tile is written: signal it, and only then put the next loads in flight (a fence or a
@@ -401,8 +435,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     float mant[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) mant[q] = ms.mant[q][t];
-    // QK of latent block b into score buffer b; blocks 0 and 1 first, the rest (and the rope, into
-    // buffer 0) once block 0 has been read out, so that warp 0 reads block 0 while block 1 runs
+    // QK of latent block b into score buffer b, the rope (stored as rope / mant_0) into buffer 0
+    // after block 0; all 36 MMAs in one batch
     if (issue_warp) {
       if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane);
       mma_ok = mma_ok && ok;
@@ -410,9 +444,14 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
           issue_qk<0, 2>(x.tmem + kSCol, dK, dQ);
+          issue_qk<kRopeChunk, 1, true>(x.tmem + kSCol, dK, dQ);
           ptx::mma_commit(&ms.s_full[0]);
           issue_qk<2, 2>(x.tmem + kSCol + 64, dK, dQ);
           ptx::mma_commit(&ms.s_full[1]);
+          issue_qk<4, 2>(x.tmem + kSCol + 128, dK, dQ);
+          ptx::mma_commit(&ms.s_full[2]);
+          issue_qk<6, 2>(x.tmem + kSCol + 192, dK, dQ);
+          ptx::mma_commit(&ms.s_full[3]);
         }
         __syncwarp();
       }
@@ -421,16 +460,14 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     float s[64];
 #pragma unroll
     for (int h = 0; h < 64; ++h) s[h] = 0.f;
-    // scores, buffers in the order they complete: block 0, block 1, then the rope (buffer 0), block 2
-    // and block 3 (one commit for the three)
+    // scores s = sum_b mant_b S_b (the rope is inside S_0), buffers in the order they complete
 #pragma unroll 1
-    for (int k = 0; k < 5; ++k) {
-      const int bb = k < 2 ? k : k == 2 ? 4 : k - 1;      // 4 = rope
-      if (k < 3) ok = ptx::mbar_wait_warp(k < 2 ? &ms.s_full[k] : &ms.r_full, ph, x.abort, lane) && ok;
+    for (int bb = 0; bb < 4; ++bb) {
+      ok = ptx::mbar_wait_warp(&ms.s_full[bb], ph, x.abort, lane) && ok;
       if (ok) {
         ptx::tc_fence_after();
-        const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : bb == 3 ? mant[3] : 1.f);
-        const uint32_t sa = x.tmem + lane_q + kSCol + 64 * (bb < 4 ? bb : 0);
+        const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : mant[3]);
+        const uint32_t sa = x.tmem + lane_q + kSCol + 64 * bb;
         uint32_t r0[32], r1[32];
         ptx::tmem_ld32(sa, r0);
         ptx::tmem_ld32(sa + 32, r1);
@@ -439,25 +476,6 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
         for (int h = 0; h < 32; ++h) {
           s[h] = fmaf(f, __uint_as_float(r0[h]), s[h]);
           s[32 + h] = fmaf(f, __uint_as_float(r1[h]), s[32 + h]);
-        }
-      }
-      if (k == 0) {
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&ms.s_free0);
-        if (issue_warp) {
-          // buffer 0 is free once every warp has read block 0 out of it
-          mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.s_free0, ph, x.abort, lane);
-          if (mma_ok) {
-            ptx::tc_fence_after();
-            if (ptx::elect_one()) {
-              issue_qk<kRopeChunk, 1>(x.tmem + kSCol, dK, dQ);
-              issue_qk<4, 2>(x.tmem + kSCol + 128, dK, dQ);
-              issue_qk<6, 2>(x.tmem + kSCol + 192, dK, dQ);
-              ptx::mma_commit(&ms.r_full);
-            }
-            __syncwarp();
-          }
         }
       }
     }
@@ -673,9 +691,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   if (threadIdx.x == 0) {
     ptx::mbar_init(&ms.q_ready, kSoftWarps);
     ptx::mbar_init(&ms.tile_full, kGatherWarps);
-    for (int bb = 0; bb < 2; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
-    ptx::mbar_init(&ms.s_free0, kSoftWarps);
-    ptx::mbar_init(&ms.r_full, 1);
+    for (int bb = 0; bb < 4; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
     ptx::mbar_init(&ms.pv0_done, 1);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
