@@ -28,8 +28,9 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsp
   __shared__ float w_s[kMaxCombineSplit];
   __shared__ float lse_s;
   // launched as a programmatic dependent of the split kernel: its partials are complete and visible
-  // only after this wait (a no-op for an ordinary launch)
+  // only after this wait (a no-op for an ordinary launch); the next split kernel may be scheduled now
   ptx::griddep_wait();
+  if (tid == 0) ptx::griddep_launch_dependents();
   const float4* rows = reinterpret_cast<const float4*>(o_part + ((size_t)b * nsplit * H + h) * kDLatent) + tid;
   const size_t split_stride = (size_t)H * kDLatent / 4;      // float4s between partitions of a row
   float4 v[kBatch];

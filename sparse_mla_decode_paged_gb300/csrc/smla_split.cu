@@ -674,6 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
 
   if (x.n_tiles == 0) {
     // empty partition: out = 0, lse = -inf
+    ptx::griddep_wait();
     for (int i = threadIdx.x; i < x.hg_valid * kDLatent; i += kThreads) {
       const size_t h = (size_t)x.g * kHeads + i / kDLatent;
       const int d = i % kDLatent;
@@ -708,6 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   __syncthreads();
   ptx::tc_fence_after();
   x.tmem = ms.tmem_slot;
+  // launched as a programmatic dependent: the setup above overlapped the previous kernel's tail;
+  // nothing in global memory (inputs it may have written, partials it may still read) is touched
+  // before that kernel has completed
+  ptx::griddep_wait();
 
   if (warp >= kSoftWarps) gather_role(x, warp, lane);
   else softmax_role(x, warp, lane);
@@ -777,8 +782,19 @@ cudaError_t launch_split(const SplitParams& p, cudaStream_t stream) {
   }
   const int head_groups = (p.H + kHeads - 1) / kHeads;
   dim3 grid(p.nsplit, head_groups, p.B);
-  split_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the CTAs may be scheduled, and set up, while the previous
+  // kernel in the stream drains; they wait for it (griddep_wait) before touching global memory
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, split_kernel, p);
 }
 
 }  // namespace smla
