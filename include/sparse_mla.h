@@ -87,12 +87,14 @@ typedef struct smla_dims {
   int32_t d_rope;             /* must be 64                                              */
   int32_t nsplit;             /* partitions of the top-k list; 0 = scheduler's choice    */
   int64_t num_pages;          /* pages in kv_cache, >= 1                                 */
+  int32_t heads_per_cta;      /* heads per CTA of the split kernel: 16, 32 or 64; 0 =    */
+                              /* scheduler's choice                                      */
 } smla_dims;
 
 typedef struct smla_plan {
   int32_t nsplit;             /* partitions of the top-k list                            */
   int32_t tokens_per_split;   /* top-k entries per partition (last may be shorter)       */
-  int32_t head_groups;        /* groups of 64 heads per (query, partition)               */
+  int32_t head_groups;        /* groups of heads_per_cta heads per (query, partition)    */
   int32_t ctas;               /* grid size of the split kernel: one CTA per (query,      */
                               /* partition, head group)                                  */
   int32_t ctas_per_sm;        /* CTAs of the split kernel resident per SM                */
@@ -100,12 +102,16 @@ typedef struct smla_plan {
   double waves;               /* ctas / (sm_count * ctas_per_sm)                         */
   double est_us;              /* cost-model estimate of one call, microseconds           */
   size_t workspace_bytes;     /* bytes sparse_mla_decode needs with this plan            */
+  int32_t heads_per_cta;      /* heads per CTA of the split kernel: 16, 32 or 64 (<= H)  */
 } smla_plan;
 
 /* Split-count scheduler, host only, no CUDA calls.  Chooses nsplit (unless
- * dims->nsplit > 0 fixes it) by minimising a wave-quantised cost model over
- * nsplit in [1, 16]: whole waves of CTAs on sm_count SMs times the per-CTA
- * time, plus the partial-result traffic and the merge.  Returns
+ * dims->nsplit > 0 fixes it) and the heads per CTA (unless
+ * dims->heads_per_cta > 0 fixes it; chosen among 16, 32, 64 up to H) by
+ * minimising a wave-quantised cost model over both: whole waves of CTAs on
+ * sm_count SMs times the per-CTA time, plus the partial-result traffic and
+ * the merge.  sparse_mla_decode and sparse_mla_split use the heads per CTA
+ * this returns for their dims.  Returns
  * SMLA_ERR_INVALID_ARG for null pointers or sm_count < 1, SMLA_ERR_UNSUPPORTED
  * for shapes outside smla_dims' stated ranges.  "The Commit That Rewrote the
  * Bottleneck", "The Levers"; "Inside the Decode Performance Investigation",

@@ -40,12 +40,14 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
 
 
-def make_dims(B: int, H: int, topk: int, max_pages_per_seq: int, num_pages: int, nsplit: int = 0) -> SmlaDims:
-    return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages)
+def make_dims(B: int, H: int, topk: int, max_pages_per_seq: int, num_pages: int, nsplit: int = 0,
+              heads_per_cta: int = 0) -> SmlaDims:
+    return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages, heads_per_cta)
 
 
-def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0) -> SmlaDims:
-    return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit)
+def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0, heads_per_cta: int = 0) -> SmlaDims:
+    return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit,
+                     heads_per_cta)
 
 
 def plan_for(dims: SmlaDims, sm_count: int) -> SmlaPlan:
@@ -87,11 +89,12 @@ def _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens):
 def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, topk_idx: torch.Tensor,
                       seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                      nsplit: int = 0, stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0 lets the library's scheduler choose."""
+                      nsplit: int = 0, stream=None, heads_per_cta: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
+    """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0 and heads_per_cta = 0 let the library's
+    scheduler choose."""
     _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
     B, H = q.shape[0], q.shape[1]
-    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit)
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta)
     if nsplit == 0:
         nsplit = plan(dims, q.device.index).nsplit
         dims.nsplit = nsplit
@@ -109,11 +112,11 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
 
 
 def sparse_mla_split(q, kv_cache, block_table, topk_idx, seq_lens, sm_scale: float, nsplit: int,
-                     err_word: Optional[torch.Tensor] = None, stream=None):
+                     err_word: Optional[torch.Tensor] = None, stream=None, heads_per_cta: int = 0):
     """Partials: o_part fp32 [B,nsplit,H,512], lse_part fp32 [B,nsplit,H]."""
     _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
     B, H = q.shape[0], q.shape[1]
-    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit)
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta)
     o_part = torch.empty((B, nsplit, H, D_LATENT), dtype=torch.float32, device=q.device)
     lse_part = torch.empty((B, nsplit, H), dtype=torch.float32, device=q.device)
     check("sparse_mla_split", _lib().sparse_mla_split(

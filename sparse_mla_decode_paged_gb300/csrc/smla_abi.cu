@@ -16,6 +16,7 @@ int check_dims(const smla_dims* d) {
   if (!d) return SMLA_ERR_INVALID_ARG;
   if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1 || d->nsplit < 0)
     return SMLA_ERR_INVALID_ARG;
+  if (d->heads_per_cta != 0 && !split_heads_supported(d->heads_per_cta)) return SMLA_ERR_INVALID_ARG;
   if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
   if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
   if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
@@ -36,7 +37,17 @@ int sm_count_of_current_device(int* sms) {
   return SMLA_OK;
 }
 
-SplitParams make_params(const smla_dims* d, int nsplit, const void* q, const void* kv, const int32_t* bt,
+// The scheduler's plan for dims with nsplit fixed (> 0) or chosen (0), on the current device.
+int plan_on_current_device(const smla_dims* dims, int nsplit, smla_plan* plan) {
+  int sms = 0;
+  const int st = sm_count_of_current_device(&sms);
+  if (st != SMLA_OK) return st;
+  smla_dims d = *dims;
+  d.nsplit = nsplit;
+  return sparse_mla_plan_for(&d, sms, plan);
+}
+
+SplitParams make_params(const smla_dims* d, int nsplit, int nh, const void* q, const void* kv, const int32_t* bt,
                         const int32_t* topk, const int32_t* seq, float sm_scale) {
   SplitParams p{};
   p.q = static_cast<const uint16_t*>(q);
@@ -51,6 +62,7 @@ SplitParams make_params(const smla_dims* d, int nsplit, const void* q, const voi
   p.max_pages = d->max_pages_per_seq;
   p.num_pages = d->num_pages;
   p.nsplit = nsplit;
+  p.nh = nh;
   p.split_len = (d->topk + nsplit - 1) / nsplit;
   return p;
 }
@@ -76,7 +88,11 @@ extern "C" int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const voi
   if (nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
   if (!o_part || !lse_part || !aligned(o_part, 16) || !aligned(lse_part, 4)) return SMLA_ERR_INVALID_ARG;
   if (err_word && !aligned(err_word, 4)) return SMLA_ERR_INVALID_ARG;
-  SplitParams p = make_params(dims, nsplit, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale);
+  smla_plan plan;
+  st = plan_on_current_device(dims, nsplit, &plan);
+  if (st != SMLA_OK) return st;
+  SplitParams p = make_params(dims, nsplit, plan.heads_per_cta, q, kv_cache, block_table, topk_idx, seq_lens,
+                              sm_scale);
   p.o_part = o_part;
   p.lse_part = lse_part;
   p.err = err_word;
@@ -93,20 +109,20 @@ extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const voi
   st = check_inputs(q, kv_cache, block_table, topk_idx, seq_lens);
   if (st != SMLA_OK) return st;
   if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return SMLA_ERR_INVALID_ARG;
-  int nsplit = dims->nsplit;
-  if (nsplit == 0) {
-    int sms = 0;
-    st = sm_count_of_current_device(&sms);
-    if (st != SMLA_OK) return st;
-    smla_plan plan;
-    st = sparse_mla_plan_for(dims, sms, &plan);
-    if (st != SMLA_OK) return st;
-    nsplit = plan.nsplit;
+  // a fixed split count fixes the workspace size: checked before the device is queried for the plan
+  if (dims->nsplit > 0) {
+    const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, dims->nsplit);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
   }
+  smla_plan plan;
+  st = plan_on_current_device(dims, dims->nsplit, &plan);
+  if (st != SMLA_OK) return st;
+  const int nsplit = plan.nsplit;
   const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, nsplit);
   if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(workspace);
-  SplitParams p = make_params(dims, nsplit, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale);
+  SplitParams p = make_params(dims, nsplit, plan.heads_per_cta, q, kv_cache, block_table, topk_idx, seq_lens,
+                              sm_scale);
   p.err = reinterpret_cast<uint32_t*>(ws);
   p.out = static_cast<uint16_t*>(out);
   p.lse = lse;

@@ -29,6 +29,7 @@ struct SplitParams {
   int B, H, topk_n, max_pages;
   int64_t num_pages;
   int nsplit;
+  int nh;                     // heads per CTA (16, 32 or 64): H is split into ceil(H / nh) groups
   int split_len;              // top-k positions per partition
   bool final_out;             // true: write out/lse directly (nsplit == 1); false: partials
   uint16_t* out;              // bf16 [B][H][512]
@@ -51,8 +52,8 @@ cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int
 bool split_shape_supported(int H, int topk);
 // Resident CTAs per SM of the split kernel for H heads (occupancy of its smem/threads).
 int split_ctas_per_sm(int H);
-// Heads handled by one work unit of the split kernel (H is split into ceil(H / this) groups).
-int split_heads_per_cta();
+// Heads per CTA the split kernel is built for (16, 32, 64).
+bool split_heads_supported(int nh);
 // CTAs per work unit (one unit per query, partition and head group).
 int split_ctas_per_unit();
 

@@ -246,6 +246,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 }
 
 // 32 lanes x 16 consecutive 32-bit columns (store).
+// 32 lanes x 16 consecutive 32-bit columns (load).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+               : SMLA_R8(0), SMLA_R8(8)
+               : "r"(taddr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -280,6 +287,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
 __device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
+}
+
+// As sw128_desc for a swizzle span of 128, 64 or 32 bytes (layout type 2, 4 or 6 at bits 61..63).
+__device__ __forceinline__ uint64_t swz_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, int span_bytes) {
+  const uint64_t layout = span_bytes == 128 ? 2ull : span_bytes == 64 ? 4ull : 6ull;
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (layout << 61);
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, fp16 A and B, given

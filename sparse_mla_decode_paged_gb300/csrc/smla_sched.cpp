@@ -15,15 +15,18 @@
 
 namespace smla {
 
-// Cost-model constants (microseconds) of the split kernel on GB300, fitted to its measured times: a
-// fixed per-CTA latency (launch, index chain, Q and first record loads, epilogue), a per-tile cost with
-// a part that scales with the top-k entries of the tile (record loads and conversion), the extra cost
-// of fp32 partial rows over the bf16 output, and the merge kernel.
+// Cost-model constants (microseconds) of the split kernel on GB300, fitted to its measured times, for
+// CTAs of 64, 32 and 16 heads: a fixed per-CTA latency (launch, index chain, Q and first record loads)
+// plus the epilogue (NH output rows), a per-tile cost with a part that scales with the top-k entries
+// of the tile (record loads and conversion, which bound a tile at every NH), the extra cost of fp32
+// partial rows over the bf16 output, and the merge kernel.  Fitted to graph-replay sweeps of every
+// (nsplit, NH) on the five workloads (model vs measured within ~15%).
 struct CostModel {
-  double cta_fixed_us = 13.0;
-  double tile_fixed_us = 3.3;
-  double tile_token_us = 3.0 / 128;
-  double partial_extra_us = 0.7;       // 128 KB of fp32 partial rows instead of 64 KB of bf16 output
+  double cta_fixed_us = 8.3;
+  double epilogue_us_per_head = 3.6 / 64;
+  double tile_fixed_us[3] = {2.0, 2.3, 2.9};              // NH = 16, 32, 64
+  double tile_token_us[3] = {3.0 / 128, 3.0 / 128, 3.1 / 128};
+  double partial_extra_us_per_head = 0.7 / 64;         // fp32 partial rows instead of bf16 output
   double combine_fixed_us = 2.0;       // merge kernel: launch (overlapped with the split kernel's tail)
   double combine_gbs = 6000.0;
 };
@@ -34,6 +37,8 @@ static bool dims_valid(const smla_dims* d) {
   if (!d) return false;
   if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1) return false;
   if (d->nsplit < 0) return false;
+  if (d->heads_per_cta != 0 && d->heads_per_cta != 16 && d->heads_per_cta != 32 && d->heads_per_cta != 64)
+    return false;
   return true;
 }
 
@@ -54,18 +59,21 @@ size_t workspace_bytes_for(int B, int H, int nsplit) {
   return bytes;
 }
 
-static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len,
+static int nh_index(int nh) { return nh == 16 ? 0 : nh == 32 ? 1 : 2; }
+
+static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len, int nh,
                           int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
-  const int hpc = split_heads_per_cta();
-  const int head_groups = (H + hpc - 1) / hpc;
+  const int head_groups = (H + nh - 1) / nh;
   const int ctas = B * head_groups * nsplit * split_ctas_per_unit();
   const double slots = (double)sm_count * ctas_per_sm;
   const double waves = ctas / slots;
   const int whole_waves = (int)ceil(waves - 1e-9);
   const int tokens = split_len < topk ? split_len : topk;
-  double cta_us = m.cta_fixed_us;
-  for (int left = tokens; left > 0; left -= 128) cta_us += m.tile_fixed_us + m.tile_token_us * (left < 128 ? left : 128);
-  if (nsplit > 1) cta_us += m.partial_extra_us;
+  const int k = nh_index(nh);
+  double cta_us = m.cta_fixed_us + m.epilogue_us_per_head * nh;
+  for (int left = tokens; left > 0; left -= 128)
+    cta_us += m.tile_fixed_us[k] + m.tile_token_us[k] * (left < 128 ? left : 128);
+  if (nsplit > 1) cta_us += m.partial_extra_us_per_head * nh;
   double t = whole_waves * cta_us;
   if (nsplit > 1) {
     const double bytes = (double)B * H * (nsplit * (kDLatent * 4.0 + 4.0) + kDLatent * 2.0 + 4.0);
@@ -87,25 +95,33 @@ extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla
   const CostModel m;
   const int B = dims->batch, H = dims->num_heads, K = dims->topk;
   const int cps = split_ctas_per_sm(H);
-  int best_n = -1, best_len = 0, best_ctas = 0;
+  int best_n = -1, best_len = 0, best_ctas = 0, best_nh = 0;
   double best_t = 0, best_w = 0;
   int lo = 1, hi = kMaxSplit;
   if (dims->nsplit > 0) lo = hi = dims->nsplit;
-  for (int n = lo; n <= hi; ++n) {
-    const int len = split_len_for(K, n);
-    // an automatic choice never leaves a partition empty; a fixed one is kept as given
-    if (dims->nsplit == 0 && (K + len - 1) / len != n) continue;
-    int ctas;
-    double w;
-    const double t = estimate_us(m, B, H, K, n, len, sm_count, cps, &ctas, &w);
-    if (best_n < 0 || t < best_t - 1e-9) {
-      best_n = n; best_len = len; best_t = t; best_ctas = ctas; best_w = w;
+  // heads per CTA from the largest down, partitions from the fewest up: ties keep fewer CTAs
+  static const int kNh[3] = {64, 32, 16};
+  for (int a = 0; a < 3; ++a) {
+    const int nh = kNh[a];
+    if (!split_heads_supported(nh)) continue;
+    if (dims->heads_per_cta > 0 ? nh != dims->heads_per_cta : nh > H) continue;
+    for (int n = lo; n <= hi; ++n) {
+      const int len = split_len_for(K, n);
+      // an automatic choice never leaves a partition empty; a fixed one is kept as given
+      if (dims->nsplit == 0 && (K + len - 1) / len != n) continue;
+      int ctas;
+      double w;
+      const double t = estimate_us(m, B, H, K, n, len, nh, sm_count, cps, &ctas, &w);
+      if (best_n < 0 || t < best_t - 1e-9) {
+        best_n = n; best_len = len; best_t = t; best_ctas = ctas; best_w = w; best_nh = nh;
+      }
     }
   }
   memset(plan, 0, sizeof(*plan));
   plan->nsplit = best_n;
   plan->tokens_per_split = best_len;
-  plan->head_groups = (H + split_heads_per_cta() - 1) / split_heads_per_cta();
+  plan->heads_per_cta = best_nh;
+  plan->head_groups = (H + best_nh - 1) / best_nh;
   plan->ctas = best_ctas;
   plan->ctas_per_sm = cps;
   plan->sm_count = sm_count;

@@ -1,54 +1,44 @@
 // Split kernel (sm_103a): tcgen05 MMAs with TMEM accumulators, exact scores.
 //
-// One CTA per (partition s of the top-k list, group of 64 heads, query b); the
-// partition is walked in tiles of 128 top-k entries (MMA M = 128 tokens,
-// N = 64 heads).  ("The 64-Block Barrier", "The Split-K Prescription":
-// dequantise, QK^T over 576 dims, online softmax, PV over 512 dims, split-K.)
+// One CTA per (partition s of the top-k list, group of NH heads, query b), NH = 16, 32 or 64 (a
+// template parameter); the partition is walked in tiles of 128 top-k entries (MMA M = 128 tokens,
+// N = NH heads).  ("The 64-Block Barrier", "The Split-K Prescription": dequantise, QK^T over 576
+// dims, online softmax, PV over 512 dims, split-K.)
 //
-// Numerics.  A block scale is split as sc = mant * 2^e with mant in [1, 2)
-// (e clamped to [-15, 7]).  The K tile holds K' = code * 2^e in fp16, exact
-// for every E4M3 code, and Q is fp16 (exact for bf16 inside the fp16 range),
-// so each 128-dim block's MMA S_b = K'_b . Q_b^T is exact up to fp32
-// accumulation; the softmax warps form  s = sum_b mant_b * S_b + S_rope  in
-// fp32 as the four block accumulators complete.  PV reads the same K' with the
-// mantissa moved onto the probabilities:  O_b^T += K'_b^T . (P * mant_b), the
-// products P * mant_b rounded to fp16.
+// Numerics.  A block scale is split as sc = mant * 2^e (e clamped to [-15, 7]; block 0: [-30, 7], so
+// that its mant >= 1).  The K tile holds K' = code * 2^e in fp16, exact for every E4M3 code, and Q is
+// fp16 (exact for bf16 inside the fp16 range), so each 128-dim block's MMA S_b = K'_b . Q_b^T is
+// exact up to fp32 accumulation.  The rope rows are stored as rope / mant_0 and accumulate into
+// S_0 (one fp16 rounding on the rope part); the softmax warps form  s = sum_b mant_b * S_b  in fp32
+// as the four block accumulators complete.  PV reads the same K' with the mantissa moved onto the
+// probabilities:  O_b^T += K'_b^T . (P * mant_b), the products P * mant_b rounded to fp16.
 //
 // Warp roles (12 warps, one CTA per SM):
-//   gather (8 warps)   warp g owns tokens [16g, 16g + 16) of a tile.  Lanes
-//                      0..15 resolve index -> row through the block table
-//                      (a1) as a three-stage pipeline: the top-k entries of
-//                      tile i + 2, the block-table entries of tile i + 1 and
-//                      the record bytes of tile i + 1 are in flight while tile
-//                      i is converted (all issued where they are written, so
-//                      no load waits on another).  The record bytes are read
-//                      coalesced: one token's 512 code bytes per warp load,
-//                      four tokens' rope bytes, sixteen tokens' scales.  Codes
-//                      -> K' (fp16, 128B-swizzled chunks of 64 dims), rope
-//                      bf16 -> fp16, mantissas and validity to shared memory.
-//                      A warp signals its part of the tile (mbarrier) before
-//                      it issues the next loads: a fence or barrier after them
-//                      would wait for them.
-//   MMA issue          thread 0 (a softmax thread, which has no loads in
-//                      flight): QK block b into score buffer b (b = 0..3), the
-//                      rope into buffer 0 once block 0 has been read out, and
-//                      the PV MMAs.
-//   softmax (4 warps)  one token (TMEM lane) per thread, 64 heads: scores
-//                      accumulated from the score buffers as they complete,
-//                      lazy running max (a head's reference moves only when a
-//                      score exceeds it by more than 2^8; O and the row sums
-//                      are then rescaled), P = exp2(s - m), row sums reduced
-//                      over the warp.  PV runs block by block: P * mant_b is
-//                      written into the rope chunk or chunk 0 of the K tile
-//                      (each free once the MMAs reading it are done: the rope
-//                      QK, resp. the PV of block 0) and thread 0 issues that
-//                      block's 8 MMAs, so writing P * mant_{b+1} overlaps PV
-//                      of block b.
-//   epilogue (all)     O / l from TMEM written straight to the [head][512] output
-//                      rows (two dims per lane and store), lse.
+//   gather (8 warps)   warp g owns tokens [16g, 16g + 16) of a tile.  Lanes 0..15 resolve index ->
+//                      row through the block table (a1) in a four-stage pipeline: top-k entries of
+//                      tile i + 4 and block-table entries of tile i + 3 in flight, the records of tile
+//                      i + 3 bulk-prefetched into L2 while those of tile i + 1 are loaded into
+//                      registers (all issued where they are written, so no load waits on another).
+//                      Record bytes are read coalesced: one token's 512 code bytes per warp load,
+//                      four tokens' rope bytes, sixteen tokens' scales.  Codes -> K' (fp16,
+//                      128B-swizzled chunks of 64 dims), rope bf16 / mant_0 -> fp16, mantissas and
+//                      validity to shared memory.  A warp signals its part of the tile (mbarrier)
+//                      before it issues the next loads: a fence or barrier after them would wait for
+//                      them.
+//   MMA issue          one elected lane of softmax warp 0, from unrolled issuers whose descriptors
+//                      are a base plus a compile-time offset: the 36 QK MMAs of a tile in one batch
+//                      (block b into score buffer b, the rope into block 0's), then the PV MMAs.
+//   softmax (4 warps)  one token (TMEM lane) per thread, NH heads: scores accumulated from the score
+//                      buffers as they complete, lazy running max (a head's reference moves only
+//                      when a score exceeds it by more than 2^8; O and the row sums are then
+//                      rescaled), P = exp2(s - m), row sums reduced over the warp.  PV: P * mant_0
+//                      into the rope chunk, block 0's 8 MMAs; then P * mant_1..3 into chunks 0, 1
+//                      and the rope chunk (free once block 0's PV is done) and the other 24 MMAs.
+//   epilogue (all)     O / l from TMEM written straight to the [head][512] output rows (two dims per
+//                      lane and store), lse.
 //
-// Shared memory: Q 72 KB + K tile 144 KB + ~4 KB; TMEM: O^T in columns
-// 0..255 (4 blocks x 64 heads), score buffers in 256..511.
+// Shared memory: Q 9 * 128 * NH bytes (18, 36 or 72 KB) + K tile 144 KB + ~5 KB; TMEM: 8 * NH
+// columns, O^T in 0 .. 4 NH - 1 (4 blocks x NH heads), score buffers in 4 NH .. 8 NH - 1.
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
@@ -59,28 +49,41 @@ namespace smla {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kHeads = 64;
+constexpr int kHeadsMax = 64;
 constexpr int kThreads = 384;
 constexpr int kSoftWarps = 4;
 constexpr int kSoftThreads = 32 * kSoftWarps;     // warps 0..3: TMEM lane quadrants 0..3
 constexpr int kGatherWarps = 8;
 constexpr int kTokPerGatherWarp = kTile / kGatherWarps;   // 16
-constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kSCol = 256;                   // score buffer b at 256 + 64 b
 constexpr float kRescaleThreshold = 8.0f;         // log2 units: P <= 2^8
 constexpr float kFp16Max = 65504.0f;
 constexpr float kMaxScale = 16384.0f;             // P * mant <= 2^8 * 2^7 stays inside fp16
 
-constexpr uint32_t kQChunk = kHeads * 128;        // 64 heads x 64 dims fp16
 constexpr uint32_t kKChunk = kTile * 128;         // 128 tokens x 64 dims fp16
-constexpr uint32_t kQBytes = 9 * kQChunk;         // 73728
-constexpr uint32_t kKBase = kQBytes;
 constexpr uint32_t kKBytes = 9 * kKChunk;         // 147456
 constexpr uint32_t kRopeChunk = 8;
-constexpr uint32_t kMiscOff = kKBase + kKBytes;
 
-constexpr uint32_t kIdescQK = ptx::idesc_f16(128, kHeads, 0, 0);
-constexpr uint32_t kIdescPV = ptx::idesc_f16(128, kHeads, 1, 1);
+// Per head-group size NH: Q chunks of NH rows x 64 dims, TMEM columns, MMA N, and the P * mant
+// buffers ([128 tokens][NH heads] fp16, MN-major with NH * 2-byte rows: a 128-, 64- or 32-byte
+// swizzle span).
+template <int NH>
+struct Cfg {
+  static_assert(NH == 16 || NH == 32 || NH == 64, "heads per CTA");
+  static constexpr uint32_t kQChunk = NH * 128;
+  static constexpr uint32_t kQBytes = 9 * kQChunk;
+  static constexpr uint32_t kKBase = kQBytes;               // a multiple of 1024
+  static constexpr uint32_t kMiscOff = kKBase + kKBytes;
+  static constexpr uint32_t kTmemCols = 8 * NH;             // 128, 256, 512
+  static constexpr uint32_t kSCol = 4 * NH;                 // score buffer b at 4 NH + NH b
+  static constexpr uint32_t kIdescQK = ptx::idesc_f16(128, NH, 0, 0);
+  static constexpr uint32_t kIdescPV = ptx::idesc_f16(128, NH, 1, 1);
+  static constexpr int kPRow = 2 * NH;                      // bytes of one token's P * mant row
+  static constexpr int kPUnits = NH / 8;                    // 16-byte units per row
+  static constexpr uint32_t kPStep = 16 * kPRow;            // bytes of 16 tokens (one PV MMA's K)
+  static constexpr int kR = NH >= 32 ? NH / 32 : 1;         // heads per lane after a reduce-scatter
+  static constexpr int kChunkCols = NH >= 32 ? 32 : 16;     // TMEM columns per O^T chunk
+  static constexpr int kChunks = 4 * NH / kChunkCols;       // O^T chunks
+};
 
 struct Misc {
   uint64_t q_ready;          // Q staged (one arrival per softmax warp)
@@ -94,16 +97,26 @@ struct Misc {
   int range_err;
   alignas(16) float mant[4][kTile];
   unsigned char valid[kTile];
-  alignas(16) float m_ref[kHeads];       // reference max per head, log2 units
-  alignas(16) float m_new[kHeads];
-  alignas(16) float alpha[kHeads];
-  alignas(16) float red[kSoftWarps][kHeads];
-  alignas(16) float linv[kHeads];
-  float lse_out[kHeads];
+  alignas(16) float m_ref[kHeadsMax];    // reference max per head, log2 units
+  alignas(16) float m_new[kHeadsMax];
+  alignas(16) float alpha[kHeadsMax];
+  alignas(16) float red[kSoftWarps][kHeadsMax];
+  alignas(16) float linv[kHeadsMax];
+  float lse_out[kHeadsMax];
 };
 
-constexpr size_t kSmemBytes = 1024 + kMiscOff + sizeof(Misc);
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+template <int NH>
+constexpr size_t smem_bytes() { return 1024 + Cfg<NH>::kMiscOff + sizeof(Misc); }
+static_assert(smem_bytes<64>() <= 232448, "shared memory per CTA");
+
+// Byte offset of 16-byte unit u of row r in a buffer of `row_bytes`-wide rows with the matching
+// swizzle (128, 64 or 32 bytes): the unit index is XOR-ed with the row's bits above the span.
+template <int kRowBytes>
+__device__ __forceinline__ uint32_t swz_row(uint32_t row, uint32_t unit) {
+  constexpr uint32_t mask = kRowBytes / 16 - 1;
+  constexpr int shift = kRowBytes == 128 ? 0 : kRowBytes == 64 ? 1 : 2;
+  return row * kRowBytes + ((unit ^ ((row >> shift) & mask)) << 4);
+}
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
   return row * 128u + ((unit ^ (row & 7u)) << 4);
@@ -115,25 +128,26 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
 // rebuilding each descriptor on that thread costs more than the MMA itself.
 //
 // QK of chunks [ch0, ch0 + nch) into one score buffer.
-template <int kCh0, int kNch, bool kAccumulate = false>
+template <int NH, int kCh0, int kNch, bool kAccumulate = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dK, uint64_t dQ) {
 #pragma unroll
   for (int cc = 0; cc < kNch; ++cc)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk)
       ptx::mma_f16_ss(d_tmem, dK + (uint64_t)(((kCh0 + cc) * kKChunk + 32 * kk) >> 4),
-                      dQ + (uint64_t)(((kCh0 + cc) * kQChunk + 32 * kk) >> 4), kIdescQK,
+                      dQ + (uint64_t)(((kCh0 + cc) * Cfg<NH>::kQChunk + 32 * kk) >> 4), Cfg<NH>::kIdescQK,
                       (kAccumulate || cc != 0 || kk != 0) ? 1u : 0u);
 }
 
 // PV of latent block kB: O^T_b (+)= K'_b^T . (P * mant_b); A is the K tile read MN-major (dims of
 // chunks 2b, 2b + 1), B the 16-token slices of the P * mant buffer.
-template <int kB>
+template <int NH, int kB>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t dV, uint64_t dBuf, bool accumulate) {
 #pragma unroll
   for (int kk = 0; kk < kTile / 16; ++kk)
-    ptx::mma_f16_ss(tmem + 64 * kB, dV + (uint64_t)((2 * kB * kKChunk + kk * 2048) >> 4),
-                    dBuf + (uint64_t)((kk * 2048) >> 4), kIdescPV, (accumulate || kk > 0) ? 1u : 0u);
+    ptx::mma_f16_ss(tmem + NH * kB, dV + (uint64_t)((2 * kB * kKChunk + kk * 2048) >> 4),
+                    dBuf + (uint64_t)((kk * Cfg<NH>::kPStep) >> 4), Cfg<NH>::kIdescPV,
+                    (accumulate || kk > 0) ? 1u : 0u);
 }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
@@ -199,35 +213,53 @@ __device__ __forceinline__ int64_t shfl_i64(int64_t v, int src) {
   return (int64_t)(((uint64_t)(uint32_t)hi << 32) | (uint32_t)lo);
 }
 
-// Warp reduce-scatter over 64 per-thread values: afterwards lane l holds the reduction over the
-// warp's 32 threads of columns 2l and 2l+1 (62 shuffles; v is kept).
-template <bool kMax>
-__device__ __forceinline__ float2 reduce_scatter64(const float (&v)[64], int lane) {
-  float a[32];
+// Warp reduce-scatter over NH per-thread values.  Each level halves the values a lane keeps (the lane
+// with the level's bit set keeps the upper half) until kR remain; levels left over reduce across the
+// lane pair.  Afterwards lane l holds the reduction over the warp's 32 threads of heads
+// kR l .. kR l + kR - 1 (NH >= 32), or of head l / 2 (NH = 16, on lanes l and l ^ 1).
+template <bool kMax, int NH>
+__device__ __forceinline__ void reduce_scatter(const float (&v)[NH], int lane, float (&out)[Cfg<NH>::kR]) {
+  constexpr int R = Cfg<NH>::kR;
+  float a[NH / 2];
   {
     const bool hi = lane & 16;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float send = hi ? v[i] : v[32 + i];
-      const float keep = hi ? v[32 + i] : v[i];
+    for (int i = 0; i < NH / 2; ++i) {
+      const float send = hi ? v[i] : v[NH / 2 + i];
+      const float keep = hi ? v[NH / 2 + i] : v[i];
       const float r = __shfl_xor_sync(0xffffffffu, send, 16);
       a[i] = kMax ? fmaxf(keep, r) : keep + r;
     }
   }
+  int span = NH / 2;
 #pragma unroll
-  for (int span = 16, x = 8; span >= 2; span >>= 1, x >>= 1) {
-    const bool hi = lane & x;
+  for (int x = 8; x >= 1; x >>= 1) {
+    if (span > R) {
+      const int half = span / 2;
+      const bool hi = lane & x;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i < span) {
-        const float send = hi ? a[i] : a[span + i];
-        const float keep = hi ? a[span + i] : a[i];
-        const float r = __shfl_xor_sync(0xffffffffu, send, x);
-        a[i] = kMax ? fmaxf(keep, r) : keep + r;
+      for (int i = 0; i < NH / 4; ++i) {
+        if (i < half) {
+          const float send = hi ? a[i] : a[half + i];
+          const float keep = hi ? a[half + i] : a[i];
+          const float r = __shfl_xor_sync(0xffffffffu, send, x);
+          a[i] = kMax ? fmaxf(keep, r) : keep + r;
+        }
       }
+      span = half;
+    } else {
+      const float r = __shfl_xor_sync(0xffffffffu, a[0], x);
+      a[0] = kMax ? fmaxf(a[0], r) : a[0] + r;
     }
   }
-  return make_float2(a[0], a[1]);
+#pragma unroll
+  for (int r = 0; r < R; ++r) out[r] = a[r];
+}
+
+// Head of value r a lane holds after reduce_scatter.
+template <int NH>
+__device__ __forceinline__ int rs_head(int lane, int r) {
+  return NH >= 32 ? Cfg<NH>::kR * lane + r : lane >> 1;
 }
 
 struct Ctx {
@@ -387,7 +419,10 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
 }
 
 // ------------------------------------------------------------------------------------------ softmax
+template <int NH>
 __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
+  using C = Cfg<NH>;
+  constexpr int R = C::kR;
   const SplitParams& p = *x.p;
   Misc& ms = *x.ms;
   const int t = threadIdx.x;                 // token of the tile = TMEM lane
@@ -397,21 +432,23 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   bool ok = true, mma_ok = true;
 
   {
-    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads
-    const uint16_t* qg = p.q + ((size_t)x.b * p.H + (size_t)x.g * kHeads) * kDQK;
+    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads: NH rows x 72 16-byte units
+    const uint16_t* qg = p.q + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDQK;
+    constexpr int kUnits = NH * 72 / kSoftThreads;   // per thread: 9, 18 or 36
+    constexpr int kBatch = kUnits < 18 ? kUnits : 18;
 #pragma unroll 1
-    for (int k0 = 0; k0 < 36; k0 += 18) {
-      uint4 v[18];
+    for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
+      uint4 v[kBatch];
 #pragma unroll
-      for (int k = 0; k < 18; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
         v[k] = n < x.hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j)
                               : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
-      for (int k = 0; k < 18; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
-        ptx::sts128_async_only(x.q_base + (j >> 3) * kQChunk + swz128(n, j & 7), bf8_to_h8(v[k], range_bad));
+        ptx::sts128_async_only(x.q_base + (j >> 3) * C::kQChunk + swz128(n, j & 7), bf8_to_h8(v[k], range_bad));
       }
     }
     ptx::fence_proxy_async_smem();
@@ -420,13 +457,17 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   }
 
   const float c2 = p.sm_scale * 1.4426950408889634f;
-  float lsum0 = 0.f, lsum1 = 0.f;            // this warp's row sums of heads 2 lane, 2 lane + 1
+  float lsum[R];                             // this warp's row sums of the heads rs_head(lane, r)
+#pragma unroll
+  for (int r = 0; r < R; ++r) lsum[r] = 0.f;
   const uint32_t bufR = x.k_base + kRopeChunk * kKChunk, buf0 = x.k_base, buf1 = x.k_base + kKChunk;
   const uint64_t dK = ptx::sw128_desc(x.k_base, 16, 1024), dQ = ptx::sw128_desc(x.q_base, 16, 1024);
   const uint64_t dV = ptx::sw128_desc(x.k_base, kKChunk, 1024);   // K tile as the MN-major A of PV
-  // P * mant buffers as MN-major B: one 64-head atom along N, so the leading offset is never stepped
-  const uint64_t dBufR = ptx::sw128_desc(bufR, 1024, 1024), dBuf0 = ptx::sw128_desc(buf0, 1024, 1024),
-                 dBuf1 = ptx::sw128_desc(buf1, 1024, 1024);
+  // P * mant buffers as MN-major B: one NH-head swizzle span along N (the leading offset is never
+  // stepped), 8-token groups 8 * row bytes apart
+  const uint64_t dBufR = ptx::swz_desc(bufR, 8 * C::kPRow, 8 * C::kPRow, C::kPRow),
+                 dBuf0 = ptx::swz_desc(buf0, 8 * C::kPRow, 8 * C::kPRow, C::kPRow),
+                 dBuf1 = ptx::swz_desc(buf1, 8 * C::kPRow, 8 * C::kPRow, C::kPRow);
 
   for (int i = 0; i < x.n_tiles; ++i) {
     const uint32_t ph = i & 1;
@@ -443,23 +484,23 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       if (mma_ok) {
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          issue_qk<0, 2>(x.tmem + kSCol, dK, dQ);
-          issue_qk<kRopeChunk, 1, true>(x.tmem + kSCol, dK, dQ);
+          issue_qk<NH, 0, 2>(x.tmem + C::kSCol, dK, dQ);
+          issue_qk<NH, kRopeChunk, 1, true>(x.tmem + C::kSCol, dK, dQ);
           ptx::mma_commit(&ms.s_full[0]);
-          issue_qk<2, 2>(x.tmem + kSCol + 64, dK, dQ);
+          issue_qk<NH, 2, 2>(x.tmem + C::kSCol + NH, dK, dQ);
           ptx::mma_commit(&ms.s_full[1]);
-          issue_qk<4, 2>(x.tmem + kSCol + 128, dK, dQ);
+          issue_qk<NH, 4, 2>(x.tmem + C::kSCol + 2 * NH, dK, dQ);
           ptx::mma_commit(&ms.s_full[2]);
-          issue_qk<6, 2>(x.tmem + kSCol + 192, dK, dQ);
+          issue_qk<NH, 6, 2>(x.tmem + C::kSCol + 3 * NH, dK, dQ);
           ptx::mma_commit(&ms.s_full[3]);
         }
         __syncwarp();
       }
     }
     __syncwarp();
-    float s[64];
+    float s[NH];
 #pragma unroll
-    for (int h = 0; h < 64; ++h) s[h] = 0.f;
+    for (int h = 0; h < NH; ++h) s[h] = 0.f;
     // scores s = sum_b mant_b S_b (the rope is inside S_0), buffers in the order they complete
 #pragma unroll 1
     for (int bb = 0; bb < 4; ++bb) {
@@ -467,23 +508,34 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       if (ok) {
         ptx::tc_fence_after();
         const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : mant[3]);
-        const uint32_t sa = x.tmem + lane_q + kSCol + 64 * bb;
-        uint32_t r0[32], r1[32];
-        ptx::tmem_ld32(sa, r0);
-        ptx::tmem_ld32(sa + 32, r1);
-        ptx::tmem_wait_ld();
+        const uint32_t sa = x.tmem + lane_q + C::kSCol + NH * bb;
+        if constexpr (NH == 16) {
+          uint32_t r0[16];
+          ptx::tmem_ld16(sa, r0);
+          ptx::tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < 32; ++h) {
-          s[h] = fmaf(f, __uint_as_float(r0[h]), s[h]);
-          s[32 + h] = fmaf(f, __uint_as_float(r1[h]), s[32 + h]);
+          for (int h = 0; h < 16; ++h) s[h] = fmaf(f, __uint_as_float(r0[h]), s[h]);
+        } else {
+#pragma unroll
+          for (int hh = 0; hh < NH; hh += 64) {
+            uint32_t r0[32], r1[32];
+            ptx::tmem_ld32(sa + hh, r0);
+            if (NH - hh > 32) ptx::tmem_ld32(sa + hh + 32, r1);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              s[hh + h] = fmaf(f, __uint_as_float(r0[h]), s[hh + h]);
+              if (NH - hh > 32) s[hh + 32 + h] = fmaf(f, __uint_as_float(r1[h]), s[hh + 32 + h]);
+            }
+          }
         }
       }
     }
 #pragma unroll
-    for (int h = 0; h < 64; ++h) s[h] = (ok && valid) ? s[h] : -CUDART_INF_F;
+    for (int h = 0; h < NH; ++h) s[h] = (ok && valid) ? s[h] : -CUDART_INF_F;
     bool need = false;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < NH / 4; ++k) {
       const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
       need |= (s[4 * k] > m.x + kRescaleThreshold) | (s[4 * k + 1] > m.y + kRescaleThreshold) |
               (s[4 * k + 2] > m.z + kRescaleThreshold) | (s[4 * k + 3] > m.w + kRescaleThreshold);
@@ -491,14 +543,14 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     need = ptx::named_bar_or(3, kSoftThreads, need);
     if (need) {
       // a head's reference max moves to its tile max when that exceeds it by more than the threshold
-      const float2 mx = reduce_scatter64<true>(s, lane);
-      ms.red[warp][2 * lane] = mx.x;
-      ms.red[warp][2 * lane + 1] = mx.y;
+      float mx[R];
+      reduce_scatter<true, NH>(s, lane, mx);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (NH >= 32 || (lane & 1) == 0) ms.red[warp][rs_head<NH>(lane, r)] = mx[r];
       ptx::named_bar_sync(2, kSoftThreads);
       if (warp == 0) {
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int h = 2 * lane + e;
+        for (int h = lane; h < NH; h += 32) {
           const float tm = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
           const float mo = ms.m_ref[h];
           const float mn = tm > mo + kRescaleThreshold ? tm : mo;
@@ -507,33 +559,42 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
         }
       }
       ptx::named_bar_sync(2, kSoftThreads);
-      lsum0 *= ms.alpha[2 * lane];
-      lsum1 *= ms.alpha[2 * lane + 1];
+#pragma unroll
+      for (int r = 0; r < R; ++r) lsum[r] *= ms.alpha[rs_head<NH>(lane, r)];
       if (i > 0 && ok) {
         // O of the previous tiles (their PV is complete: this tile's K was written after it)
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
-          uint32_t r[32];
-          const uint32_t oa = x.tmem + lane_q + 32 * c;
-          ptx::tmem_ld32(oa, r);
-          ptx::tmem_wait_ld();
+        for (int c = 0; c < C::kChunks; ++c) {
+          const uint32_t oa = x.tmem + lane_q + C::kChunkCols * c;
+          const int h0 = (C::kChunkCols * c) % NH;
+          if constexpr (NH == 16) {
+            uint32_t r[16];
+            ptx::tmem_ld16(oa, r);
+            ptx::tmem_wait_ld();
 #pragma unroll
-          for (int h = 0; h < 32; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * ms.alpha[32 * (c & 1) + h]);
-          ptx::tmem_st32(oa, r);
+            for (int h = 0; h < 16; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * ms.alpha[h]);
+            ptx::tmem_st16(oa, r);
+          } else {
+            uint32_t r[32];
+            ptx::tmem_ld32(oa, r);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) r[h] = __float_as_uint(__uint_as_float(r[h]) * ms.alpha[h0 + h]);
+            ptx::tmem_st32(oa, r);
+          }
         }
         ptx::tmem_wait_st();
       }
       ptx::named_bar_sync(2, kSoftThreads);
       if (warp == 0) {
-        ms.m_ref[2 * lane] = ms.m_new[2 * lane];
-        ms.m_ref[2 * lane + 1] = ms.m_new[2 * lane + 1];
+        for (int h = lane; h < NH; h += 32) ms.m_ref[h] = ms.m_new[h];
       }
       ptx::named_bar_sync(2, kSoftThreads);
     }
     // P = exp2(s - m) (a head with no valid entry yet has m = -inf and P = 0), fp16 pairs
-    uint32_t ph2[32];
+    uint32_t ph2[NH / 2];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
+    for (int k = 0; k < NH / 4; ++k) {
       const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
       const float mm[4] = {m.x, m.y, m.z, m.w};
 #pragma unroll
@@ -545,15 +606,16 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       ph2[2 * k + 1] = f32x2_to_f16x2_sat(s[4 * k + 2], s[4 * k + 3]);
     }
 
-    // PV block by block: P * mant_b into the rope chunk (b = 0, 2) or chunk 0 (b = 1, 3), each free
-    // once the MMAs reading it are done (the rope QK, resp. the PV of block 0)
+    // PV: P * mant_0 into the rope chunk (free: the QK is complete), block 0's 8 MMAs; then P * mant
+    // of blocks 1..3 into chunks 0 and 1 and the rope chunk (free once block 0's PV is done)
     auto write_pm = [&](int bb, uint32_t buf) {
       const float mb = bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : mant[3];
       const uint32_t m2 = f32x2_to_f16x2_sat(mb, mb);
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        ptx::sts128_async_only(buf + swz128(t, u), make_uint4(hmul2(ph2[4 * u], m2), hmul2(ph2[4 * u + 1], m2),
-                                                              hmul2(ph2[4 * u + 2], m2), hmul2(ph2[4 * u + 3], m2)));
+      for (int u = 0; u < C::kPUnits; ++u)
+        ptx::sts128_async_only(buf + swz_row<C::kPRow>(t, u),
+                               make_uint4(hmul2(ph2[4 * u], m2), hmul2(ph2[4 * u + 1], m2),
+                                          hmul2(ph2[4 * u + 2], m2), hmul2(ph2[4 * u + 3], m2)));
     };
     write_pm(0, bufR);
     ptx::fence_proxy_async_smem();
@@ -564,7 +626,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       if (mma_ok) {
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          issue_pv<0>(x.tmem, dV, dBufR, i > 0);
+          issue_pv<NH, 0>(x.tmem, dV, dBufR, i > 0);
           ptx::mma_commit(&ms.pv0_done);
         }
         __syncwarp();
@@ -572,12 +634,12 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     }
     // row sums, while block 0's PV runs
     {
-      const float2 ps = reduce_scatter64<false>(s, lane);
-      lsum0 += ps.x;
-      lsum1 += ps.y;
+      float ps[R];
+      reduce_scatter<false, NH>(s, lane, ps);
+#pragma unroll
+      for (int r = 0; r < R; ++r) lsum[r] += ps[r];
     }
     ok = ptx::mbar_wait_warp(&ms.pv0_done, ph, x.abort, lane) && ok;
-    // block 0's PV is done: chunks 0 and 1 and the rope chunk take P * mant of blocks 1..3
     write_pm(1, buf0);
     write_pm(2, bufR);
     write_pm(3, buf1);
@@ -586,9 +648,9 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     if (issue_warp && mma_ok) {
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        issue_pv<1>(x.tmem, dV, dBuf0, i > 0);
-        issue_pv<2>(x.tmem, dV, dBufR, i > 0);
-        issue_pv<3>(x.tmem, dV, dBuf1, i > 0);
+        issue_pv<NH, 1>(x.tmem, dV, dBuf0, i > 0);
+        issue_pv<NH, 2>(x.tmem, dV, dBufR, i > 0);
+        issue_pv<NH, 3>(x.tmem, dV, dBuf1, i > 0);
         ptx::mma_commit(&ms.pv_done);
       }
       __syncwarp();
@@ -599,40 +661,45 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     if (ptx::elect_one()) ptx::mma_commit(&ms.teardown);
     __syncwarp();
   }
-  ms.red[warp][2 * lane] = lsum0;
-  ms.red[warp][2 * lane + 1] = lsum1;
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+    if (NH >= 32 || (lane & 1) == 0) ms.red[warp][rs_head<NH>(lane, r)] = lsum[r];
 }
 
 // ------------------------------------------------------------------------------------------ epilogue
 // All 12 warps write O / l from TMEM straight to the output rows [head][512] (bf16, or fp32
 // partials): warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and the
-// 32-column chunks c = w / 4, w / 4 + 3, ... of O^T (chunk c: block c / 2, heads 32 (c % 2) ..).
-// Lanes 2j, 2j + 1 hold dims d, d + 1; for heads h, h + 1 the even lane writes row h and the odd lane
-// row h + 1, two dims each, so a warp store covers two 64- (bf16) or 128-byte (fp32) row segments.
+// column chunks c = w / 4, w / 4 + 3, ... of O^T (chunks of 32 columns, 16 for NH = 16; block
+// c * cols / NH).  Lanes 2j, 2j + 1 hold dims d, d + 1; for heads h, h + 1 the even lane writes row h
+// and the odd lane row h + 1, two dims each.
+template <int NH>
 __device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane) {
+  using C = Cfg<NH>;
+  constexpr int kCols = C::kChunkCols;
   const SplitParams& p = *x.p;
   Misc& ms = *x.ms;
   const int quad = warp & 3;
   const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
   const bool odd = lane & 1;
-  const size_t head0 = (size_t)x.g * kHeads;
+  const size_t head0 = (size_t)x.g * NH;
 #pragma unroll 1
-  for (int c = warp >> 2; c < 8; c += 3) {
-    const int jb = c >> 1, hb = 32 * (c & 1);
-    uint32_t r[32];
-    ptx::tmem_ld32(x.tmem + lane_q + 32 * c, r);
-    float v[32];
+  for (int c = warp >> 2; c < C::kChunks; c += 3) {
+    const int jb = (kCols * c) / NH, hb = (kCols * c) % NH;
+    uint32_t r[kCols];
+    if constexpr (kCols == 16) ptx::tmem_ld16(x.tmem + lane_q + kCols * c, r);
+    else ptx::tmem_ld32(x.tmem + lane_q + kCols * c, r);
+    float v[kCols];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
+    for (int k = 0; k < kCols / 4; ++k) {
       const float4 l4 = reinterpret_cast<const float4*>(ms.linv + hb)[k];
       v[4 * k] = l4.x; v[4 * k + 1] = l4.y; v[4 * k + 2] = l4.z; v[4 * k + 3] = l4.w;
     }
     ptx::tmem_wait_ld();
 #pragma unroll
-    for (int h = 0; h < 32; ++h) v[h] *= __uint_as_float(r[h]);
+    for (int h = 0; h < kCols; ++h) v[h] *= __uint_as_float(r[h]);
     const int d0 = 128 * jb + 32 * quad + (lane & ~1);
 #pragma unroll
-    for (int h = 0; h < 32; h += 2) {
+    for (int h = 0; h < kCols; h += 2) {
       const float mine = odd ? v[h + 1] : v[h];
       const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
       const float lo = odd ? other : mine, hi = odd ? mine : other;   // dims d0, d0 + 1
@@ -650,10 +717,12 @@ __device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane)
   }
 }
 
+template <int NH>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p) {
+  using C = Cfg<NH>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Misc& ms = *reinterpret_cast<Misc*>(base + kMiscOff);
+  Misc& ms = *reinterpret_cast<Misc*>(base + C::kMiscOff);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the merge (launched as a programmatic dependent) may be scheduled now: it waits for this grid
   if (threadIdx.x == 0) ptx::griddep_launch_dependents();
@@ -663,26 +732,26 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   x.ms = &ms;
   x.abort = &ms.abort;
   x.q_base = ptx::smem_u32(base);
-  x.k_base = x.q_base + kKBase;
+  x.k_base = x.q_base + C::kKBase;
   x.split = blockIdx.x;
   x.g = blockIdx.y;
   x.b = blockIdx.z;
   x.pos0 = x.split * p.split_len;
   x.pos_end = min(x.pos0 + p.split_len, p.topk_n);
   x.n_tiles = x.pos_end > x.pos0 ? (x.pos_end - x.pos0 + kTile - 1) / kTile : 0;
-  x.hg_valid = min(kHeads, p.H - kHeads * x.g);
+  x.hg_valid = min(NH, p.H - NH * x.g);
 
   if (x.n_tiles == 0) {
     // empty partition: out = 0, lse = -inf
     ptx::griddep_wait();
     for (int i = threadIdx.x; i < x.hg_valid * kDLatent; i += kThreads) {
-      const size_t h = (size_t)x.g * kHeads + i / kDLatent;
+      const size_t h = (size_t)x.g * NH + i / kDLatent;
       const int d = i % kDLatent;
       if (p.final_out) p.out[((size_t)x.b * p.H + h) * kDLatent + d] = 0;
       else p.o_part[(((size_t)x.b * p.nsplit + x.split) * p.H + h) * kDLatent + d] = 0.f;
     }
     if ((int)threadIdx.x < x.hg_valid) {
-      const size_t h = (size_t)x.g * kHeads + threadIdx.x;
+      const size_t h = (size_t)x.g * NH + threadIdx.x;
       if (p.final_out) p.lse[(size_t)x.b * p.H + h] = -CUDART_INF_F;
       else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = -CUDART_INF_F;
     }
@@ -700,9 +769,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     ms.range_err = 0;
     ptx::fence_mbar_init();
   }
-  if (threadIdx.x < kHeads) ms.m_ref[threadIdx.x] = -CUDART_INF_F;
+  if (threadIdx.x < kHeadsMax) ms.m_ref[threadIdx.x] = -CUDART_INF_F;
   if (warp == 0) {
-    ptx::tmem_alloc(&ms.tmem_slot, kTmemCols);
+    ptx::tmem_alloc(&ms.tmem_slot, C::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::tc_fence_before();
@@ -715,13 +784,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   ptx::griddep_wait();
 
   if (warp >= kSoftWarps) gather_role(x, warp, lane);
-  else softmax_role(x, warp, lane);
+  else softmax_role<NH>(x, warp, lane);
 
   // ------------------------------------------------------------------ epilogue
   bool ok = ptx::mbar_wait_warp(&ms.pv_done, (x.n_tiles - 1) & 1, x.abort, lane);
   ptx::tc_fence_after();
   __syncthreads();                           // row sums of the softmax warps are in ms.red
-  if (threadIdx.x < kHeads) {
+  if (threadIdx.x < NH) {
     const int h = threadIdx.x;
     const float L = ms.red[0][h] + ms.red[1][h] + ms.red[2][h] + ms.red[3][h];
     ms.linv[h] = L > 0.f ? 1.f / L : 0.f;
@@ -730,10 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   __syncthreads();
   const bool out_ok = ok && !ms.abort;
   if (out_ok) {
-    epilogue_write(x, warp, lane);
+    epilogue_write<NH>(x, warp, lane);
     if ((int)threadIdx.x < x.hg_valid) {
       const int hl = threadIdx.x;
-      const size_t h = (size_t)x.g * kHeads + hl;
+      const size_t h = (size_t)x.g * NH + hl;
       if (p.final_out) p.lse[(size_t)x.b * p.H + h] = ms.lse_out[hl];
       else p.lse_part[((size_t)x.b * p.nsplit + x.split) * p.H + h] = ms.lse_out[hl];
     }
@@ -752,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     }
   }
   __syncthreads();
-  if (warp == 0) ptx::tmem_dealloc(x.tmem, kTmemCols);
+  if (warp == 0) ptx::tmem_dealloc(x.tmem, C::kTmemCols);
 }
 
 }  // namespace
@@ -761,7 +830,7 @@ bool split_shape_supported(int H, int topk) {
   return (H == 16 || H == 32 || H == 64 || H == 128) && topk >= 1 && topk <= kMaxTopk;
 }
 
-int split_heads_per_cta() { return kHeads; }
+bool split_heads_supported(int nh) { return nh == 16 || nh == 32 || nh == 64; }
 
 int split_ctas_per_unit() { return 1; }
 
@@ -770,31 +839,45 @@ int split_ctas_per_sm(int H) {
   return 1;
 }
 
-cudaError_t launch_split(const SplitParams& p, cudaStream_t stream) {
+namespace {
+
+template <int NH>
+cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
   static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  const int head_groups = (p.H + kHeads - 1) / kHeads;
+  const int head_groups = (p.H + NH - 1) / NH;
   dim3 grid(p.nsplit, head_groups, p.B);
   // programmatic stream serialization: the CTAs may be scheduled, and set up, while the previous
   // kernel in the stream drains; they wait for it (griddep_wait) before touching global memory
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = smem_bytes<NH>();
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, split_kernel, p);
+  return cudaLaunchKernelEx(&cfg, split_kernel<NH>, p);
+}
+
+}  // namespace
+
+cudaError_t launch_split(const SplitParams& p, cudaStream_t stream) {
+  switch (p.nh) {
+    case 16: return launch_split_nh<16>(p, stream);
+    case 32: return launch_split_nh<32>(p, stream);
+    case 64: return launch_split_nh<64>(p, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace smla

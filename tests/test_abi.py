@@ -84,7 +84,8 @@ def test_plan_fields_consistent(lib):
             assert 1 <= p.nsplit <= 16
             assert p.tokens_per_split == math.ceil(512 / p.nsplit)
             assert math.ceil(512 / p.tokens_per_split) == p.nsplit          # no empty partition
-            assert p.head_groups == max(1, math.ceil(H / 64))
+            assert p.heads_per_cta in (16, 32, 64) and p.heads_per_cta <= H
+            assert p.head_groups == math.ceil(H / p.heads_per_cta)
             assert p.ctas == B * p.head_groups * p.nsplit
             assert abs(p.waves - p.ctas / (152 * p.ctas_per_sm)) < 1e-12
             ws = 256 if p.nsplit == 1 else 256 + math.ceil(B * p.nsplit * H * 4 / 256) * 256 + B * p.nsplit * H * 2048
@@ -109,6 +110,17 @@ def test_plan_is_argmin_of_its_cost_model(lib):
 def test_plan_fixed_split_kept(lib):
     p = _plan(lib, 4, 64, 10, 152, nsplit=16)
     assert p.nsplit == 16 and p.tokens_per_split == 1
+
+
+def test_plan_fixed_heads_per_cta_kept(lib):
+    for nh in (16, 32, 64):
+        for H in (16, 64, 128):
+            p = _native.SmlaPlan()
+            d = make_dims(8, H, 512, 8192, 1 << 20, 0, nh)
+            assert lib.sparse_mla_plan_for(C.byref(d), 152, C.byref(p)) == 0
+            assert p.heads_per_cta == nh and p.head_groups == math.ceil(H / nh)
+    p = _native.SmlaPlan()
+    assert lib.sparse_mla_plan_for(C.byref(make_dims(8, 64, 512, 8192, 1 << 20, 0, 48)), 152, C.byref(p)) == 1
 
 
 def test_wave_count_matches_pages_arithmetic(lib):

@@ -46,6 +46,18 @@ def test_every_split_count(nsplit):
     compare(out, lse, *oracle_on(w))
 
 
+@pytest.mark.parametrize("nh", [16, 32, 64])
+@pytest.mark.parametrize("H,nsplit", [(16, 1), (32, 3), (64, 1), (64, 4), (128, 2)])
+def test_every_head_group_size(H, nsplit, nh):
+    # the split kernel's 16-, 32- and 64-head variants on every head count (fewer heads than a group:
+    # padded rows), one partition of several tiles and several partitions
+    w = _custom(B=3, H=H, topk=400, ctx=[5000, 400, 77], seed=50 + nh + H + nsplit, outlier_channels=2)
+    out, lse = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                     nsplit=nsplit, heads_per_cta=nh)
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle_on(w))
+
+
 @pytest.mark.parametrize("H,nsplit", [(16, 4), (32, 8), (64, 5), (128, 3), (64, 2)])
 def test_split_merge_heads_and_partitions(H, nsplit):
     # head counts of one or two groups, partitions made only of padding (ctx 40 < topk), several
