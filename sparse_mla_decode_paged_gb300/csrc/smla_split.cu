@@ -850,6 +850,14 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
     if (e != cudaSuccess) return e;
+    // the smallest shared-memory carveout that holds the CTA: the rest of the SM's SRAM is L1, where the
+    // record loads in flight land (about 28 KB at 64 heads per CTA, 60 KB at 16 or 32)
+    int max_smem = 0;
+    e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    if (e != cudaSuccess) return e;
+    const int pct = (int)((100 * (smem_bytes<NH>() + 1024) + max_smem - 1) / max_smem);
+    e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributePreferredSharedMemoryCarveout, pct < 100 ? pct : 100);
+    if (e != cudaSuccess) return e;
     configured_device = dev;
   }
   const int head_groups = (p.H + NH - 1) / NH;
