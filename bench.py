@@ -258,37 +258,71 @@ class Bench:
         return reduce_max(e0.elapsed_time(e1) / 1e3, world)
 
     def e2e(self, steps: int, warmup: int):
-        """Per step: H2D of the step's inputs from pinned host memory, the decode call, D2H of out + lse."""
+        """End to end through the public API with host buffers: every step copies its inputs from pinned
+        host memory to the device, runs the decode call and reads out + lse back to pinned host memory.
+        The steps are pipelined as a serving loop would run them: copies in on one stream, the decode on
+        a second, copies out on a third, with two device buffer sets, so step i + 1's inputs and step
+        i - 1's results move while step i computes (events order each step's copy in -> decode -> copy
+        out and keep a buffer set from being overwritten before it is read)."""
         torch = self.torch
         hosts = []
         for w in self.sets[:min(self.R, 16)]:
             hosts.append(tuple(t.cpu().pin_memory() for t in (w.q, w.block_table, w.topk_idx, w.seq_lens)))
         w0 = self.w0
-        dq, dbt, dtk, dsl = (torch.empty_like(t) for t in (w0.q, w0.block_table, w0.topk_idx, w0.seq_lens))
-        out_h = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        lse_h = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        dev_in = [tuple(torch.empty_like(t) for t in (w0.q, w0.block_table, w0.topk_idx, w0.seq_lens))
+                  for _ in range(2)]
+        dev_out = [(torch.empty_like(self.out), torch.empty_like(self.lse)) for _ in range(2)]
+        wss = [self.ws, self.api.alloc_workspace(self.dims, self.nsplit, self.device)]
+        host_out = [(torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory(),
+                     torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()) for _ in range(2)]
         h2d = sum(t.numel() * t.element_size() for t in hosts[0])
-        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        d2h = host_out[0][0].numel() * 2 + host_out[0][1].numel() * 4
+        s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event()
+        copied = [ev(), ev()]                       # inputs of buffer set k on the device
+        computed = [ev(), ev()]                     # decode of buffer set k done (its inputs are free)
+        read = [ev(), ev()]                         # results of buffer set k on the host (its outputs are free)
+        started = [False, False]
 
         def step(i):
+            k = i & 1
             hq, hbt, htk, hsl = hosts[i % len(hosts)]
-            dq.copy_(hq, non_blocking=True)
-            dbt.copy_(hbt, non_blocking=True)
-            dtk.copy_(htk, non_blocking=True)
-            dsl.copy_(hsl, non_blocking=True)
-            self.api.sparse_mla_decode(dq, self.cache, dbt, dtk, dsl, w0.sm_scale, out=self.out, lse=self.lse,
-                                       workspace=self.ws, nsplit=self.nsplit)
-            out_h.copy_(self.out, non_blocking=True)
-            lse_h.copy_(self.lse, non_blocking=True)
+            dq, dbt, dtk, dsl = dev_in[k]
+            out, lse = dev_out[k]
+            with torch.cuda.stream(s_in):
+                if started[k]:
+                    s_in.wait_event(computed[k])
+                dq.copy_(hq, non_blocking=True)
+                dbt.copy_(hbt, non_blocking=True)
+                dtk.copy_(htk, non_blocking=True)
+                dsl.copy_(hsl, non_blocking=True)
+                copied[k].record(s_in)
+            with torch.cuda.stream(s_comp):
+                s_comp.wait_event(copied[k])
+                if started[k]:
+                    s_comp.wait_event(read[k])
+                self.api.sparse_mla_decode(dq, self.cache, dbt, dtk, dsl, w0.sm_scale, out=out, lse=lse,
+                                           workspace=wss[k], nsplit=self.nsplit, stream=s_comp)
+                computed[k].record(s_comp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(computed[k])
+                host_out[k][0].copy_(out, non_blocking=True)
+                host_out[k][1].copy_(lse, non_blocking=True)
+                read[k].record(s_out)
+            started[k] = True
 
         for i in range(warmup):
             step(i)
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
+        e0.record(s_in)
+        s_comp.wait_event(e0)
+        s_out.wait_event(e0)
         for i in range(steps):
-            step(i)
-        e1.record()
+            step(warmup + i)
+        s_out.wait_stream(s_in)
+        s_out.wait_stream(s_comp)
+        e1.record(s_out)
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / steps, h2d, d2h
 
