@@ -260,10 +260,13 @@ class Bench:
     def e2e(self, steps: int, warmup: int):
         """End to end through the public API with host buffers: every step copies its inputs from pinned
         host memory to the device, runs the decode call and reads out + lse back to pinned host memory.
-        The steps are pipelined as a serving loop would run them: copies in on one stream, the decode on
-        a second, copies out on a third, with two device buffer sets, so step i + 1's inputs and step
+        The steps are pipelined as a serving loop runs them: copies in on one stream, the decode on a
+        second, copies out on a third, with two device buffer sets, so step i + 1's inputs and step
         i - 1's results move while step i computes (events order each step's copy in -> decode -> copy
-        out and keep a buffer set from being overwritten before it is read)."""
+        out and keep a buffer set from being overwritten before it is read).  The loop of G steps is
+        captured once as a CUDA graph (copies and launches) and replayed, as a serving loop does to keep
+        the host's launch cost (about 15 us per decode call, measured separately) off the critical
+        path."""
         torch = self.torch
         hosts = []
         for w in self.sets[:min(self.R, 16)]:
@@ -282,15 +285,14 @@ class Bench:
         copied = [ev(), ev()]                       # inputs of buffer set k on the device
         computed = [ev(), ev()]                     # decode of buffer set k done (its inputs are free)
         read = [ev(), ev()]                         # results of buffer set k on the host (its outputs are free)
-        started = [False, False]
 
-        def step(i):
+        def step(i, first):
             k = i & 1
             hq, hbt, htk, hsl = hosts[i % len(hosts)]
             dq, dbt, dtk, dsl = dev_in[k]
             out, lse = dev_out[k]
             with torch.cuda.stream(s_in):
-                if started[k]:
+                if not first:
                     s_in.wait_event(computed[k])
                 dq.copy_(hq, non_blocking=True)
                 dbt.copy_(hbt, non_blocking=True)
@@ -299,7 +301,7 @@ class Bench:
                 copied[k].record(s_in)
             with torch.cuda.stream(s_comp):
                 s_comp.wait_event(copied[k])
-                if started[k]:
+                if not first:
                     s_comp.wait_event(read[k])
                 self.api.sparse_mla_decode(dq, self.cache, dbt, dtk, dsl, w0.sm_scale, out=out, lse=lse,
                                            workspace=wss[k], nsplit=self.nsplit, stream=s_comp)
@@ -309,20 +311,40 @@ class Bench:
                 host_out[k][0].copy_(out, non_blocking=True)
                 host_out[k][1].copy_(lse, non_blocking=True)
                 read[k].record(s_out)
-            started[k] = True
 
-        for i in range(warmup):
-            step(i)
+        def loop(n, start):
+            cur = torch.cuda.current_stream()
+            fork = ev()
+            fork.record(cur)
+            for s in (s_in, s_comp, s_out):
+                s.wait_event(fork)
+            for i in range(n):
+                step(start + i, first=i < 2)
+            for s in (s_in, s_comp, s_out):
+                cur.wait_stream(s)
+
+        loop(max(2, warmup), 0)                     # eager warm-up (and a check that the path runs)
+        torch.cuda.synchronize()
+        G = min(64, steps)
+        reps, tail = divmod(steps, G)
+        graphs = []
+        for n in ([G] + ([tail] if tail else [])):
+            g = torch.cuda.CUDAGraph()
+            cap = torch.cuda.Stream()
+            cap.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.graph(g, stream=cap):
+                loop(n, 0)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        graphs[0].replay()                          # upload
         torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
-        s_comp.wait_event(e0)
-        s_out.wait_event(e0)
-        for i in range(steps):
-            step(warmup + i)
-        s_out.wait_stream(s_in)
-        s_out.wait_stream(s_comp)
-        e1.record(s_out)
+        e0.record()
+        for _ in range(reps):
+            graphs[0].replay()
+        if tail:
+            graphs[1].replay()
+        e1.record()
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / steps, h2d, d2h
 
