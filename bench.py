@@ -213,6 +213,24 @@ class Bench:
         if st != 0:
             raise RuntimeError(f"sparse_mla_split failed: {st}")
 
+    def append_setup(self, sets: int = 8):
+        """Inputs of the KV append step at this batch: one new token per request, written into a cache
+        of its own (one page per request), latent/rope drawn per rotation."""
+        torch = self.torch
+        B = self.w0.B
+        g = torch.Generator(device="cpu").manual_seed(12345)
+        self.app_sets = [((torch.randn(B, 512, generator=g)).to(torch.bfloat16).to(self.device),
+                          torch.randn(B, 64, generator=g).to(torch.bfloat16).to(self.device),
+                          torch.full((B,), r % 64, dtype=torch.int32).to(self.device)) for r in range(sets)]
+        self.app_cache = torch.zeros((B, 64, 656), dtype=torch.uint8, device=self.device)
+        self.app_bt = torch.arange(B, dtype=torch.int32, device=self.device).reshape(B, 1)
+        # bytes per token: latent 1024 + rope 128 read, record 656 written, position + table entry 8
+        self.app_bytes = B * (1024 + 128 + 656 + 8)
+
+    def append_only(self, i: int):
+        lat, rope, pos = self.app_sets[i % len(self.app_sets)]
+        self.api.sparse_mla_kv_append(lat, rope, self.app_bt, pos, self.app_cache)
+
     def launches_per_call(self) -> int:
         return 1 + (1 if self.nsplit > 1 else 0)
 
@@ -356,11 +374,17 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
     ts = b.timed(b.split_only, steps, warmup)
     us_split = ts * 1e6 / steps
     gbs = b.bytes_per_call / (us * 1e-6) / 1e9
+    b.append_setup()
+    ta = b.timed(b.append_only, steps, warmup)
+    us_app = ta * 1e6 / steps
     res = {"us_per_call": round(us, 3), "split_kernel_us": round(us_split, 3), "nsplit": b.nsplit,
+           "heads_per_cta": b.plan.heads_per_cta,
            "ctas": b.plan.ctas, "algorithmic_bytes": b.bytes_per_call, "gbs": round(gbs, 1),
            "roofline_frac_call": round(gbs / peak_gbs, 4),
            "roofline_frac_split_kernel": round(b.bytes_per_call / (us_split * 1e-6) / 1e9 / peak_gbs, 4),
-           "rotations": b.R}
+           "rotations": b.R,
+           "kv_append": {"tokens": b.w0.B, "us_per_call": round(us_app, 3), "algorithmic_bytes": b.app_bytes,
+                         "gbs": round(b.app_bytes / (us_app * 1e-6) / 1e9, 1)}}
     del b
     import torch
     torch.cuda.empty_cache()

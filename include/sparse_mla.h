@@ -160,6 +160,43 @@ int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const void* q, const
                      float sm_scale, float* o_part, float* lse_part, uint32_t* err_word,
                      smla_stream_t stream);
 
+/* Shapes of one KV append call. */
+typedef struct smla_append_dims {
+  int32_t tokens;             /* new tokens to write, >= 0                               */
+  int32_t num_requests;       /* rows of block_table, >= 1                               */
+  int32_t page_size;          /* tokens per page; must be 64                             */
+  int32_t max_pages_per_seq;  /* row length of block_table, >= 1                         */
+  int32_t d_latent;           /* must be 512                                             */
+  int32_t d_rope;             /* must be 64                                              */
+  int64_t num_pages;          /* pages in kv_cache, >= 1                                 */
+} smla_append_dims;
+
+/* FP8 KV append: the write side of the cache sparse_mla_decode reads (the
+ * step before the decode: "Inside the Decode Performance Investigation",
+ * Task 1, paged FP8 latent cache with per-block scales).  For every new token
+ * i, with request r = requests[i] (or i when requests is NULL) and logical
+ * position t = positions[i], writes the 656-byte record at page
+ * block_table[r][t / 64], slot t % 64 of kv_cache:
+ *   scale_j = fp32(amax_j / 448) over latent dims [128 j, 128 j + 128) (1 when
+ *             the block is all zero), IEEE division;
+ *   code_d  = E4M3(fp32(latent_d / scale_{d / 128})), round to nearest even,
+ *             saturating to +-448;
+ *   record  = [code x 512 | scale x 4 (fp32, little-endian) | rope x 64 (bf16)].
+ *   latent      bf16 [tokens][512], rope bf16 [tokens][64] (16-byte aligned)
+ *   block_table int32 [num_requests][max_pages_per_seq]
+ *   requests    int32 [tokens] or NULL; positions int32 [tokens]
+ *   kv_cache    uint8 [num_pages][64][656] (written; other records untouched)
+ *   err_word    device uint32 (may be NULL): a token whose request, position
+ *               or page is out of range is skipped and sets
+ *               SMLA_DEVERR_PAGE_RANGE.
+ * Tokens that map to the same record race (the last write wins).  Returns
+ * SMLA_ERR_INVALID_ARG for null or misaligned pointers and bad shapes,
+ * SMLA_ERR_UNSUPPORTED for page_size / d_latent / d_rope other than 64 / 512
+ * / 64, SMLA_ERR_CUDA if the launch fails.  Asynchronous on `stream`. */
+int sparse_mla_kv_append(const smla_append_dims* dims, const void* latent, const void* rope,
+                         const int32_t* block_table, const int32_t* requests, const int32_t* positions,
+                         void* kv_cache, uint32_t* err_word, smla_stream_t stream);
+
 /* Log-sum-exp merge (a7) of nsplit partials:
  *   lse[b][h] = ln sum_s exp(lse_part[b][s][h])   (-inf if every partial is -inf)
  *   out[b][h][d] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h][d]  (bf16; 0 if empty)

@@ -16,6 +16,12 @@ class SmlaDims(C.Structure):
                 ("heads_per_cta", C.c_int32)]
 
 
+class SmlaAppendDims(C.Structure):
+    _fields_ = [("tokens", C.c_int32), ("num_requests", C.c_int32), ("page_size", C.c_int32),
+                ("max_pages_per_seq", C.c_int32), ("d_latent", C.c_int32), ("d_rope", C.c_int32),
+                ("num_pages", C.c_int64)]
+
+
 class SmlaPlan(C.Structure):
     _fields_ = [("nsplit", C.c_int32), ("tokens_per_split", C.c_int32), ("head_groups", C.c_int32),
                 ("ctas", C.c_int32), ("ctas_per_sm", C.c_int32), ("sm_count", C.c_int32),
@@ -28,6 +34,7 @@ _SIGS = {
     "sparse_mla_plan_for": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, C.POINTER(SmlaPlan)]),
     "sparse_mla_plan": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, C.POINTER(SmlaPlan)]),
     "sparse_mla_workspace_size": (C.c_size_t, [C.POINTER(SmlaDims), C.c_int32]),
+    "sparse_mla_kv_append": (C.c_int, [C.POINTER(SmlaAppendDims), _P, _P, _P, _P, _P, _P, _P, _P]),
     "sparse_mla_decode": (C.c_int, [C.POINTER(SmlaDims), _P, _P, _P, _P, _P, C.c_float, _P, _P, _P,
                                     C.c_size_t, _P]),
     "sparse_mla_split": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, _P, _P, _P, _P, _P, C.c_float, _P, _P,

@@ -11,7 +11,7 @@ from typing import Optional, Tuple
 import torch
 
 from . import _native
-from ._native import SmlaDims, SmlaPlan, check
+from ._native import SmlaAppendDims, SmlaDims, SmlaPlan, check
 
 PAGE_SIZE, D_LATENT, D_ROPE, D_QK = 64, 512, 64, 576
 
@@ -123,6 +123,32 @@ def sparse_mla_split(q, kv_cache, block_table, topk_idx, seq_lens, sm_scale: flo
         C.byref(dims), nsplit, _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens),
         C.c_float(sm_scale), _ptr(o_part), _ptr(lse_part), _ptr(err_word), _stream(stream)))
     return o_part, lse_part
+
+
+def sparse_mla_kv_append(latent: torch.Tensor, rope: torch.Tensor, block_table: torch.Tensor,
+                         positions: torch.Tensor, kv_cache: torch.Tensor, requests: Optional[torch.Tensor] = None,
+                         err_word: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Quantise new tokens (latent bf16 [T,512], rope bf16 [T,64]) into the paged FP8 cache at
+    (requests[i] or i, positions[i]) through block_table; kv_cache is written in place."""
+    _need(latent, "latent", torch.bfloat16, 2)
+    _need(rope, "rope", torch.bfloat16, 2)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(positions, "positions", torch.int32, 1)
+    _need(kv_cache, "kv_cache", torch.uint8, 3)
+    T = latent.shape[0]
+    if latent.shape[1] != D_LATENT or rope.shape != (T, D_ROPE) or positions.shape[0] != T:
+        raise ValueError("latent must be [T,512], rope [T,64], positions [T]")
+    if kv_cache.shape[1] != PAGE_SIZE or kv_cache.shape[2] != 656:
+        raise ValueError("kv_cache must be [pages,64,656]")
+    if requests is not None:
+        _need(requests, "requests", torch.int32, 1)
+        if requests.shape[0] != T:
+            raise ValueError("requests must be [T]")
+    dims = SmlaAppendDims(T, block_table.shape[0], PAGE_SIZE, block_table.shape[1], D_LATENT, D_ROPE,
+                          kv_cache.shape[0])
+    check("sparse_mla_kv_append", _lib().sparse_mla_kv_append(
+        C.byref(dims), _ptr(latent), _ptr(rope), _ptr(block_table), _ptr(requests), _ptr(positions),
+        _ptr(kv_cache), _ptr(err_word), _stream(stream)))
 
 
 def sparse_mla_combine(o_part: torch.Tensor, lse_part: torch.Tensor, stream=None):

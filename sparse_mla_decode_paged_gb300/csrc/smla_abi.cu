@@ -140,6 +140,35 @@ extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const voi
   return SMLA_OK;
 }
 
+extern "C" int sparse_mla_kv_append(const smla_append_dims* d, const void* latent, const void* rope,
+                                    const int32_t* block_table, const int32_t* requests, const int32_t* positions,
+                                    void* kv_cache, uint32_t* err_word, smla_stream_t stream) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->tokens < 0 || d->num_requests < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
+  if (d->tokens > 0) {
+    if (!latent || !rope || !block_table || !positions || !kv_cache) return SMLA_ERR_INVALID_ARG;
+    if (!aligned(latent, 16) || !aligned(rope, 16) || !aligned(kv_cache, 16) || !aligned(block_table, 4) ||
+        !aligned(positions, 4) || (requests && !aligned(requests, 4)))
+      return SMLA_ERR_INVALID_ARG;
+  }
+  if (err_word && !aligned(err_word, 4)) return SMLA_ERR_INVALID_ARG;
+  AppendParams p{};
+  p.latent = static_cast<const uint16_t*>(latent);
+  p.rope = static_cast<const uint16_t*>(rope);
+  p.block_table = block_table;
+  p.requests = requests;
+  p.positions = positions;
+  p.kv = static_cast<uint8_t*>(kv_cache);
+  p.tokens = d->tokens;
+  p.num_requests = d->num_requests;
+  p.max_pages = d->max_pages_per_seq;
+  p.num_pages = d->num_pages;
+  p.err = err_word;
+  return launch_kv_append(p, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
 extern "C" int sparse_mla_combine(int32_t batch, int32_t num_heads, int32_t nsplit, const float* o_part,
                                   const float* lse_part, void* out, float* lse, smla_stream_t stream) {
   if (batch < 1 || num_heads < 1 || nsplit < 1 || nsplit > kMaxCombineSplit) return SMLA_ERR_INVALID_ARG;

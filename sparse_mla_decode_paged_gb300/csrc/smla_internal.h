@@ -39,11 +39,25 @@ struct SplitParams {
   uint32_t* err;              // device error word (may be null)
 };
 
+// Everything the KV append kernel needs for one launch.
+struct AppendParams {
+  const uint16_t* latent;     // bf16 [tokens][512]
+  const uint16_t* rope;       // bf16 [tokens][64]
+  const int32_t* block_table; // [num_requests][max_pages]
+  const int32_t* requests;    // [tokens] request of each token, or null: token i belongs to request i
+  const int32_t* positions;   // [tokens] logical position of each token in its request
+  uint8_t* kv;                // [num_pages][64][656]
+  int tokens, num_requests, max_pages;
+  int64_t num_pages;
+  uint32_t* err;              // device error word (may be null)
+};
+
 // Kernel launchers (return the launch error).
 cudaError_t launch_split(const SplitParams& p, cudaStream_t stream);
 size_t workspace_bytes_for(int B, int H, int nsplit);
 cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const float* lse_part,
                            uint16_t* out, float* lse, cudaStream_t stream);
+cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens,
                                int B, int topk_n, int max_pages, int64_t num_pages, int64_t* rows,
                                cudaStream_t stream);

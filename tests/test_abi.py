@@ -131,3 +131,19 @@ def test_wave_count_matches_pages_arithmetic(lib):
     p = _plan(lib, 64, 128, 512, 188, nsplit=2)     # 2 head groups per query, as in the pages' B=64 case
     assert p.ctas == 256 and round(p.waves, 2) == round(256 / 188, 2)
     assert round(1 - oracle.wave_efficiency(p.ctas, 188), 2) == 0.32
+
+
+def test_kv_append_argument_checks_without_cuda(lib):
+    d = _native.SmlaAppendDims(4, 2, 64, 8, 512, 64, 100)
+    p = C.c_void_p(1 << 20)
+    call = lambda dims, *ptrs: lib.sparse_mla_kv_append(C.byref(dims), *ptrs)
+    ok_ptrs = [p, p, p, None, p, p, None, None]
+    assert call(d, None, p, p, None, p, p, None, None) == 1                 # null latent
+    assert call(d, C.c_void_p((1 << 20) + 8), p, p, None, p, p, None, None) == 1   # misaligned latent
+    assert call(d, p, p, p, C.c_void_p((1 << 20) + 2), p, p, None, None) == 1      # misaligned requests
+    bad = _native.SmlaAppendDims(4, 2, 32, 8, 512, 64, 100)                  # page size 32
+    assert call(bad, *ok_ptrs) == 2
+    bad = _native.SmlaAppendDims(-1, 2, 64, 8, 512, 64, 100)                 # negative token count
+    assert call(bad, *ok_ptrs) == 1
+    bad = _native.SmlaAppendDims(4, 0, 64, 8, 512, 64, 100)                  # no requests
+    assert call(bad, *ok_ptrs) == 1
