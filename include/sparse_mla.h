@@ -89,6 +89,9 @@ typedef struct smla_dims {
   int64_t num_pages;          /* pages in kv_cache, >= 1                                 */
   int32_t heads_per_cta;      /* heads per CTA of the split kernel: 16, 32 or 64; 0 =    */
                               /* scheduler's choice                                      */
+  int32_t queries_per_request;/* s_q >= 1 (0 means 1): query b reads block_table row     */
+                              /* b / s_q (several queries of one request, each with its  */
+                              /* own top-k and seq_lens entry); batch must be a multiple */
 } smla_dims;
 
 typedef struct smla_plan {
@@ -132,7 +135,7 @@ size_t sparse_mla_workspace_size(const smla_dims* dims, int32_t nsplit);
 /* Full decode: split kernel (a6) then, when nsplit > 1, the merge (a7).
  *   q           bf16 [B][H][576]
  *   kv_cache    uint8 [num_pages][64][656] (record layout above)
- *   block_table int32 [B][max_pages_per_seq]
+ *   block_table int32 [B / queries_per_request][max_pages_per_seq]
  *   topk_idx    int32 [B][topk]
  *   seq_lens    int32 [B]
  *   sm_scale    score scale (1/sqrt(576) for DeepSeek MLA)

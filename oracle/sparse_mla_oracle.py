@@ -114,11 +114,15 @@ def as_f64_q(q) -> np.ndarray:
 # ----------------------------------------------------------------------------- a1: addresses
 
 def gathered_rows(block_table, topk_idx, seq_lens, num_pages: int, page_size: int = PAGE_SIZE) -> np.ndarray:
-    """Physical row (page * page_size + slot) of every top-k entry; -1 when skipped."""
+    """Physical row (page * page_size + slot) of every top-k entry; -1 when skipped.
+
+    Query b belongs to request b // s_q, s_q = (query rows) / (block-table rows): several queries of
+    one request (each with its own top-k list and seq_lens entry) share its block-table row."""
     bt = np.asarray(block_table, dtype=np.int64)
     tk = np.asarray(topk_idx, dtype=np.int64)
     sl = np.asarray(seq_lens, dtype=np.int64)
     B, K = tk.shape
+    s_q = B // bt.shape[0]
     rows = np.full((B, K), -1, dtype=np.int64)
     for b in range(B):
         for i in range(K):
@@ -128,7 +132,7 @@ def gathered_rows(block_table, topk_idx, seq_lens, num_pages: int, page_size: in
             lp = t // page_size
             if lp >= bt.shape[1]:
                 continue
-            page = bt[b, lp]
+            page = bt[b // s_q, lp]
             if page < 0 or page >= num_pages:
                 continue
             rows[b, i] = page * page_size + (t % page_size)

@@ -13,7 +13,7 @@ class SmlaDims(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_heads", C.c_int32), ("topk", C.c_int32),
                 ("page_size", C.c_int32), ("max_pages_per_seq", C.c_int32), ("d_latent", C.c_int32),
                 ("d_rope", C.c_int32), ("nsplit", C.c_int32), ("num_pages", C.c_int64),
-                ("heads_per_cta", C.c_int32)]
+                ("heads_per_cta", C.c_int32), ("queries_per_request", C.c_int32)]
 
 
 class SmlaAppendDims(C.Structure):

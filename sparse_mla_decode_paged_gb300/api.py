@@ -41,13 +41,15 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
 
 
 def make_dims(B: int, H: int, topk: int, max_pages_per_seq: int, num_pages: int, nsplit: int = 0,
-              heads_per_cta: int = 0) -> SmlaDims:
-    return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages, heads_per_cta)
+              heads_per_cta: int = 0, queries_per_request: int = 1) -> SmlaDims:
+    return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages, heads_per_cta,
+                    queries_per_request)
 
 
 def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0, heads_per_cta: int = 0) -> SmlaDims:
+    """Shapes of a call; several queries per request when q has a multiple of block_table's rows."""
     return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit,
-                     heads_per_cta)
+                     heads_per_cta, q.shape[0] // block_table.shape[0])
 
 
 def plan_for(dims: SmlaDims, sm_count: int) -> SmlaPlan:
@@ -82,8 +84,10 @@ def _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens):
     if q.shape[2] != D_QK or kv_cache.shape[1] != PAGE_SIZE or kv_cache.shape[2] != 656:
         raise ValueError("q must be [B,H,576] and kv_cache [pages,64,656]")
     B = q.shape[0]
-    if block_table.shape[0] != B or topk_idx.shape[0] != B or seq_lens.shape[0] != B:
-        raise ValueError("batch dimensions disagree")
+    R = block_table.shape[0]
+    if R < 1 or B % R != 0 or topk_idx.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("q, topk_idx and seq_lens need one row per query, block_table one row per request "
+                         "(a divisor of the query count)")
 
 
 def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, topk_idx: torch.Tensor,
@@ -167,7 +171,9 @@ def sparse_mla_gather_rows(block_table, topk_idx, seq_lens, num_pages: int, stre
     _need(topk_idx, "topk_idx", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     B, K = topk_idx.shape
-    dims = make_dims(B, 64, K, block_table.shape[1], num_pages)
+    if block_table.shape[0] < 1 or B % block_table.shape[0] != 0:
+        raise ValueError("block_table needs one row per request (a divisor of the query count)")
+    dims = make_dims(B, 64, K, block_table.shape[1], num_pages, queries_per_request=B // block_table.shape[0])
     rows = torch.empty((B, K), dtype=torch.int64, device=topk_idx.device)
     check("sparse_mla_gather_rows", _lib().sparse_mla_gather_rows(
         C.byref(dims), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens), _ptr(rows), _stream(stream)))

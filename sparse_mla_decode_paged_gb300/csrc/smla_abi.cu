@@ -17,6 +17,8 @@ int check_dims(const smla_dims* d) {
   if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1 || d->nsplit < 0)
     return SMLA_ERR_INVALID_ARG;
   if (d->heads_per_cta != 0 && !split_heads_supported(d->heads_per_cta)) return SMLA_ERR_INVALID_ARG;
+  if (d->queries_per_request < 0 || (d->queries_per_request > 1 && d->batch % d->queries_per_request != 0))
+    return SMLA_ERR_INVALID_ARG;
   if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
   if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
   if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
@@ -63,6 +65,7 @@ SplitParams make_params(const smla_dims* d, int nsplit, int nh, const void* q, c
   p.num_pages = d->num_pages;
   p.nsplit = nsplit;
   p.nh = nh;
+  p.q_per_req = d->queries_per_request > 1 ? d->queries_per_request : 1;
   p.split_len = (d->topk + nsplit - 1) / nsplit;
   return p;
 }
@@ -189,7 +192,8 @@ extern "C" int sparse_mla_gather_rows(const smla_dims* dims, const int32_t* bloc
   if (dims->page_size != kPageSize) return SMLA_ERR_UNSUPPORTED;
   if (!block_table || !topk_idx || !seq_lens || !rows_out || !aligned(rows_out, 8)) return SMLA_ERR_INVALID_ARG;
   return launch_gather_rows(block_table, topk_idx, seq_lens, dims->batch, dims->topk, dims->max_pages_per_seq,
-                            dims->num_pages, rows_out, (cudaStream_t)stream) == cudaSuccess
+                            dims->num_pages, dims->queries_per_request > 1 ? dims->queries_per_request : 1, rows_out,
+                            (cudaStream_t)stream) == cudaSuccess
              ? SMLA_OK
              : SMLA_ERR_CUDA;
 }

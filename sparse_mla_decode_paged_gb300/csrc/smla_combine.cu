@@ -83,11 +83,11 @@ __global__ void __launch_bounds__(kCombineThreads) combine_kernel(int H, int nsp
 
 __global__ void gather_rows_kernel(const int32_t* __restrict__ bt, const int32_t* __restrict__ topk,
                                    const int32_t* __restrict__ seq_lens, int B, int topk_n, int max_pages,
-                                   int64_t num_pages, int64_t* __restrict__ rows) {
+                                   int64_t num_pages, int q_per_req, int64_t* __restrict__ rows) {
   const int64_t n = (int64_t)B * topk_n;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const int b = (int)(i / topk_n);
-    rows[i] = row_of(bt + (size_t)b * max_pages, __ldg(topk + i), __ldg(seq_lens + b), max_pages, num_pages,
+    rows[i] = row_of(bt + (size_t)(b / q_per_req) * max_pages, __ldg(topk + i), __ldg(seq_lens + b), max_pages, num_pages,
                      nullptr);
   }
 }
@@ -112,11 +112,12 @@ cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const 
 }
 
 cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens, int B, int topk_n,
-                               int max_pages, int64_t num_pages, int64_t* rows, cudaStream_t stream) {
+                               int max_pages, int64_t num_pages, int q_per_req, int64_t* rows, cudaStream_t stream) {
   const int64_t n = (int64_t)B * topk_n;
   const int threads = 256;
   const int blocks = (int)((n + threads - 1) / threads < 4096 ? (n + threads - 1) / threads : 4096);
-  gather_rows_kernel<<<blocks, threads, 0, stream>>>(bt, topk, seq_lens, B, topk_n, max_pages, num_pages, rows);
+  gather_rows_kernel<<<blocks, threads, 0, stream>>>(bt, topk, seq_lens, B, topk_n, max_pages, num_pages, q_per_req,
+                                                      rows);
   return cudaGetLastError();
 }
 

@@ -30,6 +30,7 @@ struct SplitParams {
   int64_t num_pages;
   int nsplit;
   int nh;                     // heads per CTA (16, 32 or 64): H is split into ceil(H / nh) groups
+  int q_per_req;              // queries per request: query b reads block-table row b / q_per_req
   int split_len;              // top-k positions per partition
   bool final_out;             // true: write out/lse directly (nsplit == 1); false: partials
   uint16_t* out;              // bf16 [B][H][512]
@@ -59,8 +60,8 @@ cudaError_t launch_combine(int B, int H, int nsplit, const float* o_part, const 
                            uint16_t* out, float* lse, cudaStream_t stream);
 cudaError_t launch_kv_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_gather_rows(const int32_t* bt, const int32_t* topk, const int32_t* seq_lens,
-                               int B, int topk_n, int max_pages, int64_t num_pages, int64_t* rows,
-                               cudaStream_t stream);
+                               int B, int topk_n, int max_pages, int64_t num_pages, int q_per_req,
+                               int64_t* rows, cudaStream_t stream);
 
 // Shape limits of the split kernel (checked on the host before any launch).
 bool split_shape_supported(int H, int topk);

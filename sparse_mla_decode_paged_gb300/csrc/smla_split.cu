@@ -278,7 +278,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   const int gw = warp - kSoftWarps;
   const int tl = kTokPerGatherWarp * gw + (lane & 15);   // token resolved by this lane (lanes 16.. repeat)
   const int seq_len = __ldg(p.seq_lens + x.b);
-  const int32_t* bt_row = p.block_table + (size_t)x.b * p.max_pages;
+  const int32_t* bt_row = p.block_table + (size_t)(x.b / p.q_per_req) * p.max_pages;   // the query's request
   const int32_t* tk_row = p.topk + (size_t)x.b * p.topk_n;
   const unsigned char* kv = p.kv;
   const int blk = lane >> 3;               // scale block of this lane's 16 latent dims

@@ -298,3 +298,23 @@ def test_pages_split_numbers():
     waste = 1 - oracle.wave_efficiency(oracle.pages_grid(64), g["sms"])     # 120 idle of 376 slots
     assert round(waste, 2) == g["b64_second_wave_waste"]
     assert 1 * 64 == g["bs1_grid_b_h"] and 1 * 64 * 8 == g["split_k_prescription_blocks"]
+
+
+def test_queries_per_request_share_the_request_row():
+    # several queries of one request (block table row b // s_q) equal the same queries with the row
+    # repeated per query
+    g = np.random.default_rng(21)
+    R, s_q, K, pages = 3, 2, 12, 10
+    bt = g.permutation(pages)[: R * 3].reshape(R, 3).astype(np.int32)
+    seq = np.array([150, 151, 60, 61, 190, 191], dtype=np.int32)
+    tk = np.stack([g.integers(-1, seq[b] + 5, K) for b in range(R * s_q)]).astype(np.int32)
+    rows = oracle.gathered_rows(bt, tk, seq, pages)
+    assert np.array_equal(rows, oracle.gathered_rows(np.repeat(bt, s_q, axis=0), tk, seq, pages))
+    cache = g.integers(0, 256, size=(pages, 64, 656), dtype=np.uint8)
+    cache[..., 512:528] = np.frombuffer(np.full(pages * 64 * 4, 0.01, "<f4").tobytes(), np.uint8).reshape(pages, 64, 16)
+    cache[..., :512] &= 0x77                                              # finite codes
+    cache[..., 528:] = 0
+    q = (g.standard_normal((R * s_q, 2, 576))).astype(np.float64)
+    o1, l1 = oracle.sparse_mla_decode(q, cache, bt, tk, seq, 0.05)
+    o2, l2 = oracle.sparse_mla_decode(q, cache, np.repeat(bt, s_q, axis=0), tk, seq, 0.05)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)

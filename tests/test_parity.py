@@ -67,6 +67,37 @@ def test_split_merge_heads_and_partitions(H, nsplit):
     compare(out, lse, *oracle_on(w))
 
 
+@pytest.mark.parametrize("s_q,nsplit", [(2, 0), (3, 2), (4, 1)])
+def test_several_queries_per_request(s_q, nsplit):
+    # the MTP / verify shape: s_q queries per request, each with its own top-k and causal length
+    # (query j of a request sees positions < ctx - (s_q - 1 - j)); one block-table row per request
+    R = 3
+    base = wl.make_custom(B=R, H=64, topk=200, ctx_lens=[900, 150, 1500], seed=70 + s_q, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(71 + s_q)
+    seq, rows = [], []
+    for r in range(R):
+        for j in range(s_q):
+            L = int(base.seq_lens[r]) - (s_q - 1 - j)
+            seq.append(L)
+            pick = torch.randperm(L, generator=g)[:200]
+            rows.append(torch.cat([pick, torch.full((200 - pick.numel(),), -1)]).to(torch.int32))
+    seq_lens = torch.tensor(seq, dtype=torch.int32, device=DEV)
+    topk = torch.stack(rows).to(DEV)
+    q = torch.randn((R * s_q, 64, 576), generator=g).to(torch.bfloat16).to(DEV)
+    out, lse = api.sparse_mla_decode(q, base.kv_cache, base.block_table, topk, seq_lens, base.sm_scale,
+                                     nsplit=nsplit)
+    torch.cuda.synchronize()
+    ref_o, ref_l = oracle.sparse_mla_decode(q.cpu().view(torch.int16).numpy().view(np.uint16),
+                                            base.kv_cache.cpu().numpy(), base.block_table.cpu().numpy(),
+                                            topk.cpu().numpy(), seq_lens.cpu().numpy(), base.sm_scale)
+    compare(out, lse, ref_o, ref_l)
+    rows_gpu = api.sparse_mla_gather_rows(base.block_table, topk, seq_lens, base.kv_cache.shape[0])
+    torch.cuda.synchronize()
+    assert np.array_equal(rows_gpu.cpu().numpy(), oracle.gathered_rows(base.block_table.cpu().numpy(),
+                                                                       topk.cpu().numpy(), seq_lens.cpu().numpy(),
+                                                                       base.kv_cache.shape[0]))
+
+
 def test_split_and_combine_entry_points():
     w = _custom(B=2, H=64, topk=200, ctx=[900, 150], seed=32)
     o_part, lse_part = api.sparse_mla_split(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale, 3)
@@ -95,7 +126,7 @@ def test_edge_cases_padding_empty_duplicates():
     assert torch.all(torch.isneginf(lse[4]))
 
 
-@pytest.mark.parametrize("topk,ctx", [(1, [5, 1]), (2048, [3000, 2048]), (17, [17, 400])])
+@pytest.mark.parametrize("topk,ctx", [(1, [5, 1]), (1024, [1500, 900]), (2048, [3000, 2048]), (17, [17, 400])])
 def test_topk_extremes(topk, ctx):
     w = _custom(B=2, H=64, topk=topk, ctx=ctx, seed=34 + topk)
     out, lse = _run(w)
