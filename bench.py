@@ -231,6 +231,27 @@ class Bench:
         lat, rope, pos = self.app_sets[i % len(self.app_sets)]
         self.api.sparse_mla_kv_append(lat, rope, self.app_bt, pos, self.app_cache)
 
+    def topk_setup(self):
+        """Inputs of the top-k selection step at this workload: indexer-score stand-ins (standard
+        normal, float32) over each query's context, the workload's lengths and top-k count; enough
+        rotating score sets that they exceed 4 x L2."""
+        torch = self.torch
+        from sparse_mla_decode_paged_gb300 import workloads as wl
+        w = self.w0
+        self.tk_lens = w.seq_lens
+        self.tk_cols = int(w.seq_lens.max().item())
+        set_bytes = w.B * self.tk_cols * 4
+        n_sets = int(min(256, max(4, math.ceil(4 * self.l2 / set_bytes))))
+        self.tk_sets = [wl.make_indexer_scores(w.B, self.tk_cols, seed=5000 + r, device=self.device)
+                        for r in range(n_sets)]
+        self.tk_out = torch.empty((w.B, w.topk_idx.shape[1]), dtype=torch.int32, device=self.device)
+        # scores read below each length, kept positions written, lengths read
+        self.tk_bytes = int(w.seq_lens.sum().item()) * 4 + w.B * w.topk_idx.shape[1] * 4 + w.B * 4
+
+    def topk_only(self, i: int):
+        s = self.tk_sets[i % len(self.tk_sets)]
+        self.api.sparse_mla_topk_select(s, self.tk_lens, self.tk_out.shape[1])
+
     def launches_per_call(self) -> int:
         return 1 + (1 if self.nsplit > 1 else 0)
 
@@ -377,6 +398,9 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
     b.append_setup()
     ta = b.timed(b.append_only, steps, warmup)
     us_app = ta * 1e6 / steps
+    b.topk_setup()
+    tt = b.timed(b.topk_only, steps, warmup)
+    us_tk = tt * 1e6 / steps
     res = {"us_per_call": round(us, 3), "split_kernel_us": round(us_split, 3), "nsplit": b.nsplit,
            "heads_per_cta": b.plan.heads_per_cta,
            "ctas": b.plan.ctas, "algorithmic_bytes": b.bytes_per_call, "gbs": round(gbs, 1),
@@ -384,7 +408,12 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
            "roofline_frac_split_kernel": round(b.bytes_per_call / (us_split * 1e-6) / 1e9 / peak_gbs, 4),
            "rotations": b.R,
            "kv_append": {"tokens": b.w0.B, "us_per_call": round(us_app, 3), "algorithmic_bytes": b.app_bytes,
-                         "gbs": round(b.app_bytes / (us_app * 1e-6) / 1e9, 1)}}
+                         "gbs": round(b.app_bytes / (us_app * 1e-6) / 1e9, 1)},
+           "topk_select": {"queries": b.w0.B, "positions": b.tk_cols, "k": b.tk_out.shape[1],
+                           "scores": "standard normal float32", "rotating_sets": len(b.tk_sets),
+                           "us_per_call": round(us_tk, 3), "algorithmic_bytes": b.tk_bytes,
+                           "gbs": round(b.tk_bytes / (us_tk * 1e-6) / 1e9, 1),
+                           "roofline_frac": round(b.tk_bytes / (us_tk * 1e-6) / 1e9 / peak_gbs, 4)}}
     del b
     import torch
     torch.cuda.empty_cache()

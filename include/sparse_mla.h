@@ -76,6 +76,7 @@ typedef enum smla_status {
 #define SMLA_DEVERR_PAGE_RANGE 0x1u  /* a used top-k entry mapped outside the block table or cache */
 #define SMLA_DEVERR_TIMEOUT    0x2u  /* an internal wait gave up; that call's results are invalid  */
 #define SMLA_DEVERR_RANGE      0x4u  /* q or a dequantised latent exceeded the fp16 range          */
+#define SMLA_DEVERR_LEN_RANGE  0x8u  /* a top-k selection length outside [0, num_cols] was clamped */
 
 typedef struct smla_dims {
   int32_t batch;              /* B >= 1 decode queries                                   */
@@ -199,6 +200,36 @@ typedef struct smla_append_dims {
 int sparse_mla_kv_append(const smla_append_dims* dims, const void* latent, const void* rope,
                          const int32_t* block_table, const int32_t* requests, const int32_t* positions,
                          void* kv_cache, uint32_t* err_word, smla_stream_t stream);
+
+/* Shapes of one top-k selection call. */
+typedef struct smla_topk_dims {
+  int32_t batch;          /* queries (rows of scores), >= 0                               */
+  int32_t num_cols;       /* scored positions per row, 1 .. 393216                        */
+  int64_t row_stride;     /* elements between consecutive rows of scores, >= num_cols     */
+  int32_t k;              /* positions kept per query, 1 .. 2048                           */
+  int32_t cluster_ctas;   /* CTAs per row: 0 = chosen by the library, else 1 .. 8          */
+} smla_topk_dims;
+
+/* Top-k selection over indexer scores: the step that produces topk_idx for
+ * the decode ("Inside the Decode Performance Investigation", The Setup:
+ * index_topk = 512 positions per query; the indexer launches of the per-step
+ * kernel inventory).  For query b with len = seq_lens[b] (clamped to
+ * [0, num_cols]; a clamped length sets SMLA_DEVERR_LEN_RANGE):
+ *   len <= k: topk_idx[b] = 0, 1, ..., len - 1, then -1 up to k;
+ *   len >  k: the k positions p < len of largest scores[b][p], ranked by IEEE
+ *             754 totalOrder on the float32 patterns (-0 below +0, NaNs beyond
+ *             the infinities by sign), equal patterns ranked by lower position
+ *             first; written in increasing position order.
+ *   scores   float32 [batch][row_stride] (4-byte aligned; 16-byte aligned with
+ *            row_stride % 4 == 0 takes 16-byte loads), read only below len
+ *   seq_lens int32 [batch]; topk_idx int32 [batch][k] (written)
+ *   err_word device uint32 (may be NULL).
+ * Returns SMLA_ERR_INVALID_ARG for null or misaligned pointers and bad
+ * shapes, SMLA_ERR_UNSUPPORTED for num_cols > 393216 or k > 2048 (or a fixed
+ * cluster_ctas whose chunk exceeds 49152 positions), SMLA_ERR_CUDA if the
+ * launch fails.  Asynchronous on `stream`. */
+int sparse_mla_topk_select(const smla_topk_dims* dims, const float* scores, const int32_t* seq_lens,
+                           int32_t* topk_idx, uint32_t* err_word, smla_stream_t stream);
 
 /* Log-sum-exp merge (a7) of nsplit partials:
  *   lse[b][h] = ln sum_s exp(lse_part[b][s][h])   (-inf if every partial is -inf)

@@ -5,4 +5,5 @@ this package is its thin PyTorch binding plus the seeded workload generator.
 """
 from .api import (alloc_workspace, clear_errors, dims_of, make_dims, plan, plan_for, read_errors,  # noqa: F401
                   sparse_mla_combine, sparse_mla_decode, sparse_mla_gather_rows, sparse_mla_split,
+                  sparse_mla_topk_select,
                   workspace_size)

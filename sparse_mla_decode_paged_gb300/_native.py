@@ -22,6 +22,11 @@ class SmlaAppendDims(C.Structure):
                 ("num_pages", C.c_int64)]
 
 
+class SmlaTopkDims(C.Structure):
+    _fields_ = [("batch", C.c_int32), ("num_cols", C.c_int32), ("row_stride", C.c_int64), ("k", C.c_int32),
+                ("cluster_ctas", C.c_int32)]
+
+
 class SmlaPlan(C.Structure):
     _fields_ = [("nsplit", C.c_int32), ("tokens_per_split", C.c_int32), ("head_groups", C.c_int32),
                 ("ctas", C.c_int32), ("ctas_per_sm", C.c_int32), ("sm_count", C.c_int32),
@@ -35,6 +40,7 @@ _SIGS = {
     "sparse_mla_plan": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, C.POINTER(SmlaPlan)]),
     "sparse_mla_workspace_size": (C.c_size_t, [C.POINTER(SmlaDims), C.c_int32]),
     "sparse_mla_kv_append": (C.c_int, [C.POINTER(SmlaAppendDims), _P, _P, _P, _P, _P, _P, _P, _P]),
+    "sparse_mla_topk_select": (C.c_int, [C.POINTER(SmlaTopkDims), _P, _P, _P, _P, _P]),
     "sparse_mla_decode": (C.c_int, [C.POINTER(SmlaDims), _P, _P, _P, _P, _P, C.c_float, _P, _P, _P,
                                     C.c_size_t, _P]),
     "sparse_mla_split": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, _P, _P, _P, _P, _P, C.c_float, _P, _P,

@@ -11,7 +11,7 @@ from typing import Optional, Tuple
 import torch
 
 from . import _native
-from ._native import SmlaAppendDims, SmlaDims, SmlaPlan, check
+from ._native import SmlaAppendDims, SmlaDims, SmlaPlan, SmlaTopkDims, check
 
 PAGE_SIZE, D_LATENT, D_ROPE, D_QK = 64, 512, 64, 576
 
@@ -153,6 +153,26 @@ def sparse_mla_kv_append(latent: torch.Tensor, rope: torch.Tensor, block_table: 
     check("sparse_mla_kv_append", _lib().sparse_mla_kv_append(
         C.byref(dims), _ptr(latent), _ptr(rope), _ptr(block_table), _ptr(requests), _ptr(positions),
         _ptr(kv_cache), _ptr(err_word), _stream(stream)))
+
+
+def sparse_mla_topk_select(scores: torch.Tensor, seq_lens: torch.Tensor, k: int, cluster_ctas: int = 0,
+                           err_word: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """int32 [B,k]: per query the k positions below seq_lens[b] of largest score (IEEE totalOrder,
+    ties to the lower position), in increasing order, -1 padded when seq_lens[b] <= k.
+    scores float32 [B, num_cols] with unit stride along positions."""
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    if scores.dtype != torch.float32 or scores.dim() != 2 or not scores.is_cuda:
+        raise ValueError("scores must be a float32 [B, num_cols] CUDA tensor")
+    if scores.stride(1) != 1 or (scores.shape[0] > 1 and scores.stride(0) < scores.shape[1]):
+        raise ValueError("scores rows must be contiguous")
+    B, n = scores.shape
+    if seq_lens.shape[0] != B:
+        raise ValueError("seq_lens must be [B]")
+    out = torch.empty((B, k), dtype=torch.int32, device=scores.device)
+    dims = SmlaTopkDims(B, n, scores.stride(0) if B > 1 else n, k, cluster_ctas)
+    check("sparse_mla_topk_select", _lib().sparse_mla_topk_select(
+        C.byref(dims), _ptr(scores), _ptr(seq_lens), _ptr(out), _ptr(err_word), _stream(stream)))
+    return out
 
 
 def sparse_mla_combine(o_part: torch.Tensor, lse_part: torch.Tensor, stream=None):

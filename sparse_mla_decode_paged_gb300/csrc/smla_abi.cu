@@ -172,6 +172,35 @@ extern "C" int sparse_mla_kv_append(const smla_append_dims* d, const void* laten
   return launch_kv_append(p, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
+extern "C" int sparse_mla_topk_select(const smla_topk_dims* d, const float* scores, const int32_t* seq_lens,
+                                      int32_t* topk_idx, uint32_t* err_word, smla_stream_t stream) {
+  if (!d) return SMLA_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->num_cols < 1 || d->row_stride < d->num_cols || d->k < 1 || d->cluster_ctas < 0 ||
+      d->cluster_ctas > kTopkMaxCluster)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->k > kMaxTopk || d->num_cols > kTopkMaxCluster * kTopkMaxChunk) return SMLA_ERR_UNSUPPORTED;
+  if (d->batch > 0) {
+    if (!scores || !seq_lens || !topk_idx) return SMLA_ERR_INVALID_ARG;
+    if (!aligned(scores, 4) || !aligned(seq_lens, 4) || !aligned(topk_idx, 4)) return SMLA_ERR_INVALID_ARG;
+  }
+  if (err_word && !aligned(err_word, 4)) return SMLA_ERR_INVALID_ARG;
+  if (d->batch == 0) return SMLA_OK;
+  int sms = 0;
+  const int st = sm_count_of_current_device(&sms);
+  if (st != SMLA_OK) return st;
+  TopkParams p{};
+  if (!topk_plan(d->batch, d->num_cols, sms, d->cluster_ctas, &p.csize, &p.chunk)) return SMLA_ERR_UNSUPPORTED;
+  p.scores = scores;
+  p.seq_lens = seq_lens;
+  p.out = topk_idx;
+  p.err = err_word;
+  p.stride = d->row_stride;
+  p.num_cols = d->num_cols;
+  p.k = d->k;
+  p.vec4 = aligned(scores, 16) && d->row_stride % 4 == 0;
+  return launch_topk(p, d->batch, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
 extern "C" int sparse_mla_combine(int32_t batch, int32_t num_heads, int32_t nsplit, const float* o_part,
                                   const float* lse_part, void* out, float* lse, smla_stream_t stream) {
   if (batch < 1 || num_heads < 1 || nsplit < 1 || nsplit > kMaxCombineSplit) return SMLA_ERR_INVALID_ARG;

@@ -53,6 +53,22 @@ struct AppendParams {
   uint32_t* err;              // device error word (may be null)
 };
 
+// Top-k selection (one cluster of csize CTAs per query row, chunk positions per CTA).
+constexpr int kTopkMaxCluster = 8;     // portable cluster size
+constexpr int kTopkMaxChunk = 49152;   // scores per CTA (192 KB of keys in shared memory)
+struct TopkParams {
+  const float* scores;        // [batch][stride]
+  const int32_t* seq_lens;    // [batch]
+  int32_t* out;               // [batch][k]
+  uint32_t* err;              // device error word (may be null)
+  int64_t stride;
+  int num_cols, k, chunk, csize;
+  int vec4;                   // scores 16-byte aligned and stride % 4 == 0: 16-byte loads
+};
+bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk);
+size_t topk_smem_bytes(int chunk);
+cudaError_t launch_topk(const TopkParams& p, int batch, cudaStream_t stream);
+
 // Kernel launchers (return the launch error).
 cudaError_t launch_split(const SplitParams& p, cudaStream_t stream);
 size_t workspace_bytes_for(int B, int H, int nsplit);

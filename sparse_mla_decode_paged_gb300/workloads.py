@@ -273,6 +273,35 @@ def make_custom(B: int, H: int, topk: int, ctx_lens: Sequence[int], seed: int, d
     return Workload(spec, q, kv, bt, topk_t, seq, 1.0 / math.sqrt(D_QK))
 
 
+SCORE_PATTERNS = ("normal", "relu", "ties", "special")
+
+
+def make_indexer_scores(B: int, num_cols: int, seed: int, device="cpu", pattern: str = "normal") -> torch.Tensor:
+    """float32 [B, num_cols] stand-ins for the indexer's per-position scores.
+
+    normal  standard normal (a continuous score, few ties)
+    relu    max(0, normal): half the positions score exactly 0 (a ReLU-weighted indexer's zeros)
+    ties    normal rounded to quarters: heavy ties at every rank
+    special normal with about 1% of the entries replaced by +-0, +-inf, +-NaN and subnormals
+    """
+    g = _gen(device, seed)
+    s = torch.randn((B, num_cols), generator=g, device=device, dtype=torch.float32)
+    if pattern == "normal":
+        return s
+    if pattern == "relu":
+        return torch.clamp_min(s, 0.0)
+    if pattern == "ties":
+        return torch.round(s * 4.0) / 4.0
+    if pattern == "special":
+        bits = torch.tensor([0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000,
+                             0x00000001, 0x807FFFFF], dtype=torch.int64, device=device)
+        bits = torch.where(bits >= 2 ** 31, bits - 2 ** 32, bits).to(torch.int32)
+        pick = torch.rand((B, num_cols), generator=g, device=device) < 0.01
+        which = torch.randint(0, bits.numel(), (B, num_cols), generator=g, device=device)
+        return torch.where(pick, bits[which].view(torch.float32), s)
+    raise ValueError(f"unknown score pattern {pattern!r}")
+
+
 def touched_pages(w: Workload, batch_index: Sequence[int]) -> torch.Tensor:
     """Physical pages referenced by the valid top-k entries of the given requests (sorted, unique)."""
     pages = []

@@ -147,3 +147,19 @@ def test_kv_append_argument_checks_without_cuda(lib):
     assert call(bad, *ok_ptrs) == 1
     bad = _native.SmlaAppendDims(4, 0, 64, 8, 512, 64, 100)                  # no requests
     assert call(bad, *ok_ptrs) == 1
+
+
+def test_topk_select_argument_checks_without_cuda(lib):
+    p = C.c_void_p(1 << 20)
+    call = lambda d, *ptrs: lib.sparse_mla_topk_select(C.byref(d), *ptrs)
+    D = _native.SmlaTopkDims
+    ok = [p, p, p, None, None]
+    assert call(D(4, 1000, 1000, 512, 0), None, p, p, None, None) == 1      # null scores
+    assert call(D(4, 1000, 1000, 512, 0), C.c_void_p((1 << 20) + 2), p, p, None, None) == 1   # misaligned
+    assert call(D(4, 1000, 999, 512, 0), *ok) == 1                          # stride below the row
+    assert call(D(4, 1000, 1000, 0, 0), *ok) == 1                           # k = 0
+    assert call(D(4, 0, 1000, 8, 0), *ok) == 1                              # no positions
+    assert call(D(4, 1000, 1000, 8, 9), *ok) == 1                           # cluster of 9 CTAs
+    assert call(D(4, 1000, 1000, 4096, 0), *ok) == 2                        # k beyond 2048
+    assert call(D(4, 8 * 49152 + 1, 8 * 49152 + 1, 512, 0), *ok) == 2       # row too long
+    assert call(D(0, 1000, 1000, 512, 0), None, None, None, None, None) == 0   # empty batch: nothing to do
