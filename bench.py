@@ -86,10 +86,14 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+SPLIT_KERNEL_SOURCES = ("smla_split.cu", "smla_ptx.cuh", "smla_device.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the split kernel's own sources (its translation unit and device headers)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "sparse_mla_decode_paged_gb300", "csrc", "*"))):
-        with open(f, "rb") as fh:
+    for name in SPLIT_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "sparse_mla_decode_paged_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
@@ -576,7 +580,19 @@ def main():
     ap.add_argument("--single", type=int, default=0,
                     help="profiling driver: run this many eager calls of --workload (optionally --nsplit) and exit")
     ap.add_argument("--nsplit", type=int, default=0)
+    ap.add_argument("--single-op", choices=("decode", "topk"), default="decode",
+                    help="with --single: the decode call, or the top-k selection over the workload's contexts")
     args = ap.parse_args()
+    if args.single and args.single_op == "topk":
+        import torch
+        from sparse_mla_decode_paged_gb300 import api
+        from sparse_mla_decode_paged_gb300 import workloads as wl
+        w = wl.make_workload(wl.CONFIGS[args.workload], device="cuda")
+        scores = wl.make_indexer_scores(w.B, int(w.seq_lens.max().item()), seed=5000, device="cuda")
+        for _ in range(args.single):
+            api.sparse_mla_topk_select(scores, w.seq_lens, w.topk_idx.shape[1])
+        torch.cuda.synchronize()
+        return
     if args.single:
         import torch
         from sparse_mla_decode_paged_gb300 import api
