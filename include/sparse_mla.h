@@ -204,10 +204,10 @@ int sparse_mla_kv_append(const smla_append_dims* dims, const void* latent, const
 /* Shapes of one top-k selection call. */
 typedef struct smla_topk_dims {
   int32_t batch;          /* queries (rows of scores), >= 0                               */
-  int32_t num_cols;       /* scored positions per row, 1 .. 393216                        */
+  int32_t num_cols;       /* scored positions per row, 1 .. 786432                        */
   int64_t row_stride;     /* elements between consecutive rows of scores, >= num_cols     */
   int32_t k;              /* positions kept per query, 1 .. 2048                           */
-  int32_t cluster_ctas;   /* CTAs per row: 0 = chosen by the library, else 1 .. 8          */
+  int32_t cluster_ctas;   /* CTAs per row: 0 = chosen by the library, else 1 .. 16         */
 } smla_topk_dims;
 
 /* Top-k selection over indexer scores: the step that produces topk_idx for
@@ -225,9 +225,11 @@ typedef struct smla_topk_dims {
  *   seq_lens int32 [batch]; topk_idx int32 [batch][k] (written)
  *   err_word device uint32 (may be NULL).
  * Returns SMLA_ERR_INVALID_ARG for null or misaligned pointers and bad
- * shapes, SMLA_ERR_UNSUPPORTED for num_cols > 393216 or k > 2048 (or a fixed
+ * shapes, SMLA_ERR_UNSUPPORTED for num_cols > 786432 or k > 2048 (or a fixed
  * cluster_ctas whose chunk exceeds 49152 positions), SMLA_ERR_CUDA if the
- * launch fails.  Asynchronous on `stream`. */
+ * launch fails (clusters of more than 8 CTAs, used only for rows longer than
+ * 393216 positions, need the device to co-schedule them).  Asynchronous on
+ * `stream`. */
 int sparse_mla_topk_select(const smla_topk_dims* dims, const float* scores, const int32_t* seq_lens,
                            int32_t* topk_idx, uint32_t* err_word, smla_stream_t stream);
 

@@ -54,7 +54,8 @@ struct AppendParams {
 };
 
 // Top-k selection (one cluster of csize CTAs per query row, chunk positions per CTA).
-constexpr int kTopkMaxCluster = 8;     // portable cluster size
+constexpr int kTopkPortableCluster = 8;  // cluster sizes every launch supports
+constexpr int kTopkMaxCluster = 16;      // with the non-portable cluster size attribute (rows past 8 chunks)
 constexpr int kTopkMaxChunk = 49152;   // scores per CTA (192 KB of keys in shared memory)
 struct TopkParams {
   const float* scores;        // [batch][stride]

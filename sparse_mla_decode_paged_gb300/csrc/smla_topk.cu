@@ -483,15 +483,18 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
 
 size_t topk_smem_bytes(int chunk) { return (size_t)chunk * 4 + sizeof(TkShared); }
 
-// Cluster size and chunk for rows of num_cols positions: every candidate size 1 .. 8 whose chunk fits,
-// scored by waves x per-CTA time, the latter fitted to measured sweeps on GB300 (about 4 us fixed, 0.5 ns
-// per position of the chunk for its four passes, 3.5 us for the cluster-wide exchanges of a cluster
-// of more than one CTA); ties keep the smaller cluster.
+// Cluster size and chunk for rows of num_cols positions: every candidate size 1 .. 8 whose chunk fits
+// (9 .. 16 only for rows longer than 8 full chunks), scored by waves x per-CTA time, the latter fitted
+// to measured sweeps on GB300 (about 4 us fixed, 0.5 ns per position of the chunk for its four passes,
+// 3.5 us for the cluster-wide exchanges of a cluster of more than one CTA); ties keep the smaller
+// cluster.
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk) {
   double best_t = 0;
   int best_c = 0, best_chunk = 0;
+  const bool long_rows = num_cols > kTopkPortableCluster * kTopkMaxChunk;
   for (int c = 1; c <= kTopkMaxCluster; ++c) {
     if (forced_csize > 0 && c != forced_csize) continue;
+    if (forced_csize == 0 && c > kTopkPortableCluster && !long_rows) continue;
     const int ch = ((num_cols + c - 1) / c + 511) / 512 * 512;
     if (ch > kTopkMaxChunk) continue;
     if (forced_csize == 0 && c > 1 && (size_t)(c - 1) * ch >= (size_t)num_cols) continue;  // no empty CTA
@@ -521,6 +524,8 @@ cudaError_t launch_topk(const TopkParams& p, int batch, cudaStream_t stream) {
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)topk_smem_bytes(kTopkMaxChunk));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }

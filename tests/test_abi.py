@@ -159,7 +159,7 @@ def test_topk_select_argument_checks_without_cuda(lib):
     assert call(D(4, 1000, 999, 512, 0), *ok) == 1                          # stride below the row
     assert call(D(4, 1000, 1000, 0, 0), *ok) == 1                           # k = 0
     assert call(D(4, 0, 1000, 8, 0), *ok) == 1                              # no positions
-    assert call(D(4, 1000, 1000, 8, 9), *ok) == 1                           # cluster of 9 CTAs
+    assert call(D(4, 1000, 1000, 8, 17), *ok) == 1                          # cluster of 17 CTAs
     assert call(D(4, 1000, 1000, 4096, 0), *ok) == 2                        # k beyond 2048
-    assert call(D(4, 8 * 49152 + 1, 8 * 49152 + 1, 512, 0), *ok) == 2       # row too long
+    assert call(D(4, 16 * 49152 + 1, 16 * 49152 + 1, 512, 0), *ok) == 2     # row too long
     assert call(D(0, 1000, 1000, 512, 0), None, None, None, None, None) == 0   # empty batch: nothing to do

@@ -81,7 +81,8 @@ def test_padded_row_stride():
     _check(s, lens, 512)
 
 
-@pytest.mark.parametrize("B,n,k", [(32, 32768, 512), (80, 131072, 512), (1, 8192, 512), (4, 393216, 2048)])
+@pytest.mark.parametrize("B,n,k", [(32, 32768, 512), (80, 131072, 512), (1, 8192, 512), (4, 393216, 2048),
+                                   (3, 524288, 512), (2, 786432, 1024)])
 def test_decode_sizes(B, n, k):
     s = wl.make_indexer_scores(B, n, seed=B, device=DEV, pattern="relu")
     g = torch.Generator(device="cpu").manual_seed(B)
