@@ -62,6 +62,12 @@ constexpr float kMaxScale = 16384.0f;             // P * mant <= 2^8 * 2^7 stays
 constexpr uint32_t kKChunk = kTile * 128;         // 128 tokens x 64 dims fp16
 constexpr uint32_t kKBytes = 9 * kKChunk;         // 147456
 constexpr uint32_t kRopeChunk = 8;
+// Before tile 0 is converted the K tile is idle: it receives the raw bf16 Q of the head group (up to
+// 64 x 1152 bytes at offset 0) and tile 0's raw E4M3 codes (128 x 512 bytes) by bulk copy.
+constexpr uint32_t kRawQMax = kHeadsMax * kDQK * 2;          // 73728
+constexpr uint32_t kRawLatOff = kRawQMax;
+static_assert(kRawLatOff + kTile * kDLatent <= kKBytes, "raw staging inside the K tile");
+constexpr uint32_t kGatherBar = 4;                           // named barrier of the gather warps
 
 // Per head-group size NH: Q chunks of NH rows x 64 dims, TMEM columns, MMA N, and the P * mant
 // buffers ([128 tokens][NH heads] fp16, MN-major with NH * 2-byte rows: a 128-, 64- or 32-byte
@@ -86,6 +92,9 @@ struct Cfg {
 };
 
 struct Misc {
+  uint64_t q_raw;            // raw Q landed in the K tile (bulk copy)
+  uint64_t raw0;             // tile 0's raw codes landed in the K tile (one arrival per token lane)
+  uint64_t k_free0;          // raw Q read by every softmax warp: tile 0 may be written
   uint64_t q_ready;          // Q staged (one arrival per softmax warp)
   uint64_t tile_full;        // K tile and metadata of the tile written (one arrival per gather warp)
   uint64_t s_full[4];        // score buffer b holds block b of the tile (block 0 with the rope)
@@ -317,6 +326,15 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   // contiguous segment per warp load, lane l: dims 16 l .. 16 l + 15); rope: four tokens x 128
   // bytes per load; scales: lanes 0..15, one token each.
   uint4 lat[16], rope[4], sc;
+  auto load_side = [&](int64_t r_own) {
+    const int64_t off_own = r_own >= 0 ? r_own * kRecordBytes : -1;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int64_t off = shfl_i64(off_own, 4 * k + (lane >> 3));
+      rope[k] = off >= 0 ? ptx::ldg_stream(kv + off + 528 + 16 * (lane & 7)) : make_uint4(0, 0, 0, 0);
+    }
+    sc = off_own >= 0 ? ptx::ldg_stream(kv + off_own + 512) : make_uint4(0, 0, 0, 0);
+  };
   auto load_tile = [&](int64_t r_own) {
     const int64_t off_own = r_own >= 0 ? r_own * kRecordBytes : -1;
 #pragma unroll
@@ -324,12 +342,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
       const int64_t off = shfl_i64(off_own, k);
       lat[k] = off >= 0 ? ptx::ldg_stream(kv + off + 16 * lane) : make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int64_t off = shfl_i64(off_own, 4 * k + (lane >> 3));
-      rope[k] = off >= 0 ? ptx::ldg_stream(kv + off + 528 + 16 * (lane & 7)) : make_uint4(0, 0, 0, 0);
-    }
-    sc = off_own >= 0 ? ptx::ldg_stream(kv + off_own + 512) : make_uint4(0, 0, 0, 0);
+    load_side(r_own);
   };
 
   // Records of tile i + 2 are prefetched into L2 when tile i's are loaded into registers, so the
@@ -344,8 +357,19 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   const int pg0 = page_load(t0);
   int pg1 = page_load(t1), pg2 = page_load(t2);
   int64_t row = row_from(t0, pg0);
-  prefetch_row(row);                         // the register loads below get ~28 KB of L1: the rest hit L2
-  load_tile(row);
+  // tile 0's codes by bulk copy into the idle K tile (register loads are bound by the loads an SM
+  // keeps in flight, which a cold first tile feels most); its rope and scales by register loads.  No
+  // L2 prefetch of tile 0: the bulk copies fetch its lines.
+  const uint32_t raw0 = x.k_base + kRawLatOff;
+  if (lane < 16) {
+    if (row >= 0) {
+      ptx::mbar_arrive_expect_tx(&ms.raw0, kDLatent);
+      ptx::bulk_g2s(raw0 + (uint32_t)tl * kDLatent, kv + row * kRecordBytes, kDLatent, &ms.raw0);
+    } else {
+      ptx::mbar_arrive(&ms.raw0);
+    }
+  }
+  load_side(row);
   if (x.n_tiles > 1) prefetch_row(row_from(t1, pg1));
   if (x.n_tiles > 2) prefetch_row(row_from(t2, pg2));
   int pg3 = page_load(t3);
@@ -355,6 +379,19 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     const bool valid = row >= 0;
     // the K tile is free once every PV MMA of the previous tile is done
     if (i > 0) ok = ptx::mbar_wait_warp(&ms.pv_done, (i - 1) & 1, x.abort, lane) && ok;
+    if (i == 0) {
+      // tile 0's codes from the raw copy into registers; the K tile is written only once every gather
+      // warp has read its codes and every softmax warp its raw Q
+      ok = ptx::mbar_wait_warp(&ms.raw0, 0, x.abort, lane) && ok;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const int64_t rk = shfl_i64(row, k);
+        lat[k] = (ok && rk >= 0) ? ptx::lds128(raw0 + (uint32_t)(kTokPerGatherWarp * gw + k) * kDLatent + 16u * lane)
+                                 : make_uint4(0, 0, 0, 0);
+      }
+      ptx::named_bar_sync(kGatherBar, kGatherWarps * 32);
+      ok = ptx::mbar_wait_warp(&ms.k_free0, 0, x.abort, lane) && ok;
+    }
     if (ok) {
       const float s4[4] = {__uint_as_float(sc.x), __uint_as_float(sc.y), __uint_as_float(sc.z),
                            __uint_as_float(sc.w)};
@@ -432,8 +469,9 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   bool ok = true, mma_ok = true;
 
   {
-    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads: NH rows x 72 16-byte units
-    const uint16_t* qg = p.q + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDQK;
+    // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads: NH rows x 72 16-byte units,
+    // read from the raw bf16 rows the bulk copy put at the start of the K tile (unit id at 16 id)
+    ok = ptx::mbar_wait_warp(&ms.q_raw, 0, x.abort, lane) && ok;
     constexpr int kUnits = NH * 72 / kSoftThreads;   // per thread: 9, 18 or 36
     constexpr int kBatch = kUnits < 18 ? kUnits : 18;
 #pragma unroll 1
@@ -441,9 +479,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
       uint4 v[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
-        const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
-        v[k] = n < x.hg_valid ? __ldg(reinterpret_cast<const uint4*>(qg + (size_t)n * kDQK) + j)
-                              : make_uint4(0, 0, 0, 0);
+        const int id = t + kSoftThreads * (k0 + k), n = id / 72;
+        v[k] = (ok && n < x.hg_valid) ? ptx::lds128(x.k_base + 16u * (uint32_t)id) : make_uint4(0, 0, 0, 0);
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
@@ -453,7 +490,10 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(&ms.q_ready);
+    if (lane == 0) {
+      ptx::mbar_arrive(&ms.k_free0);   // the raw Q is read: the gather warps may overwrite it
+      ptx::mbar_arrive(&ms.q_ready);
+    }
   }
 
   const float c2 = p.sm_scale * 1.4426950408889634f;
@@ -759,6 +799,9 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   }
 
   if (threadIdx.x == 0) {
+    ptx::mbar_init(&ms.q_raw, 1);
+    ptx::mbar_init(&ms.raw0, kGatherWarps * 16);
+    ptx::mbar_init(&ms.k_free0, kSoftWarps);
     ptx::mbar_init(&ms.q_ready, kSoftWarps);
     ptx::mbar_init(&ms.tile_full, kGatherWarps);
     for (int bb = 0; bb < 4; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
@@ -782,6 +825,12 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   // nothing in global memory (inputs it may have written, partials it may still read) is touched
   // before that kernel has completed
   ptx::griddep_wait();
+  if (threadIdx.x == 0) {
+    // the head group's raw Q rows (contiguous, 1152 bytes each) into the idle K tile
+    const uint32_t qbytes = (uint32_t)x.hg_valid * kDQK * 2;
+    ptx::mbar_arrive_expect_tx(&ms.q_raw, qbytes);
+    ptx::bulk_g2s(x.k_base, p.q + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDQK, qbytes, &ms.q_raw);
+  }
 
   if (warp >= kSoftWarps) gather_role(x, warp, lane);
   else softmax_role<NH>(x, warp, lane);
