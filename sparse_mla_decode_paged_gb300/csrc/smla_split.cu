@@ -863,7 +863,13 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   if (threadIdx.x == 0) {
     // every MMA has completed before TMEM is released (time limit only)
     volatile int no_abort = 0;
-    const bool drained = ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
+    bool drained = ptx::mbar_wait_bounded(&ms.teardown, 0, &no_abort, 100000000ull);
+    if (ms.abort) {
+      // a wait gave up: the first tile's bulk copies into shared memory may still be in flight, so they
+      // are waited for (time limit only) before the CTA leaves
+      drained = ptx::mbar_wait_bounded(&ms.q_raw, 0, &no_abort, 100000000ull) && drained;
+      drained = ptx::mbar_wait_bounded(&ms.raw0, 0, &no_abort, 100000000ull) && drained;
+    }
     if (p.err) {
       if (ms.abort || !drained) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
       if (ms.range_err) atomicOr(p.err, SMLA_DEVERR_RANGE);
