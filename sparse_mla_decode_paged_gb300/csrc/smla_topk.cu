@@ -487,14 +487,22 @@ size_t topk_smem_bytes(int chunk) { return (size_t)chunk * 4 + sizeof(TkShared);
 // (9 .. 16 only for rows longer than 8 full chunks), scored by waves x per-CTA time, the latter fitted
 // to measured sweeps on GB300 (about 4 us fixed, 0.5 ns per position of the chunk for its four passes,
 // 3.5 us for the cluster-wide exchanges of a cluster of more than one CTA); ties keep the smaller
-// cluster.
+// cluster.  When some size keeps every CTA on an SM of its own, only such sizes are considered: the
+// kernel is issue-bound, so two CTAs sharing an SM run at about half speed (B = 32 x 32768: 4-CTA
+// clusters 12.4 us, 8-CTA clusters 13.1 us).
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk) {
   double best_t = 0;
   int best_c = 0, best_chunk = 0;
   const bool long_rows = num_cols > kTopkPortableCluster * kTopkMaxChunk;
+  bool one_per_sm = false;  // some admissible size puts at most one CTA on each SM
+  for (int c = 1; c <= kTopkPortableCluster && forced_csize == 0 && !long_rows; ++c) {
+    const int ch = ((num_cols + c - 1) / c + 511) / 512 * 512;
+    if (ch <= kTopkMaxChunk && (long long)batch * c <= sm_count) one_per_sm = true;
+  }
   for (int c = 1; c <= kTopkMaxCluster; ++c) {
     if (forced_csize > 0 && c != forced_csize) continue;
     if (forced_csize == 0 && c > kTopkPortableCluster && !long_rows) continue;
+    if (one_per_sm && (long long)batch * c > sm_count) continue;
     const int ch = ((num_cols + c - 1) / c + 511) / 512 * 512;
     if (ch > kTopkMaxChunk) continue;
     if (forced_csize == 0 && c > 1 && (size_t)(c - 1) * ch >= (size_t)num_cols) continue;  // no empty CTA
