@@ -233,6 +233,15 @@ typedef struct smla_topk_dims {
 int sparse_mla_topk_select(const smla_topk_dims* dims, const float* scores, const int32_t* seq_lens,
                            int32_t* topk_idx, uint32_t* err_word, smla_stream_t stream);
 
+/* The launch shape sparse_mla_topk_select uses for dims on a device with
+ * sm_count SMs (host only, no CUDA call): *cluster_ctas CTAs per query row,
+ * each holding *chunk_positions positions (a multiple of 512, at most 49152,
+ * cluster_ctas x chunk_positions >= num_cols).  dims->cluster_ctas > 0 is
+ * kept as given.  Returns SMLA_ERR_INVALID_ARG for bad shapes or pointers,
+ * SMLA_ERR_UNSUPPORTED when no shape fits. */
+int sparse_mla_topk_plan_for(const smla_topk_dims* dims, int32_t sm_count, int32_t* cluster_ctas,
+                             int32_t* chunk_positions);
+
 /* Log-sum-exp merge (a7) of nsplit partials:
  *   lse[b][h] = ln sum_s exp(lse_part[b][s][h])   (-inf if every partial is -inf)
  *   out[b][h][d] = sum_s exp(lse_part[b][s][h] - lse[b][h]) * o_part[b][s][h][d]  (bf16; 0 if empty)

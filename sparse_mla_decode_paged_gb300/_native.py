@@ -41,6 +41,8 @@ _SIGS = {
     "sparse_mla_workspace_size": (C.c_size_t, [C.POINTER(SmlaDims), C.c_int32]),
     "sparse_mla_kv_append": (C.c_int, [C.POINTER(SmlaAppendDims), _P, _P, _P, _P, _P, _P, _P, _P]),
     "sparse_mla_topk_select": (C.c_int, [C.POINTER(SmlaTopkDims), _P, _P, _P, _P, _P]),
+    "sparse_mla_topk_plan_for": (C.c_int, [C.POINTER(SmlaTopkDims), C.c_int32, C.POINTER(C.c_int32),
+                                         C.POINTER(C.c_int32)]),
     "sparse_mla_decode": (C.c_int, [C.POINTER(SmlaDims), _P, _P, _P, _P, _P, C.c_float, _P, _P, _P,
                                     C.c_size_t, _P]),
     "sparse_mla_split": (C.c_int, [C.POINTER(SmlaDims), C.c_int32, _P, _P, _P, _P, _P, C.c_float, _P, _P,

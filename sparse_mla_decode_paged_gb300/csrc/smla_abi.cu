@@ -201,6 +201,21 @@ extern "C" int sparse_mla_topk_select(const smla_topk_dims* d, const float* scor
   return launch_topk(p, d->batch, (cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
+extern "C" int sparse_mla_topk_plan_for(const smla_topk_dims* d, int32_t sm_count, int32_t* cluster_ctas,
+                                        int32_t* chunk_positions) {
+  if (!d || !cluster_ctas || !chunk_positions || sm_count < 1) return SMLA_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->num_cols < 1 || d->row_stride < d->num_cols || d->k < 1 || d->cluster_ctas < 0 ||
+      d->cluster_ctas > kTopkMaxCluster)
+    return SMLA_ERR_INVALID_ARG;
+  if (d->k > kMaxTopk || d->num_cols > kTopkMaxCluster * kTopkMaxChunk) return SMLA_ERR_UNSUPPORTED;
+  int c = 0, ch = 0;
+  if (!topk_plan(d->batch > 0 ? d->batch : 1, d->num_cols, sm_count, d->cluster_ctas, &c, &ch))
+    return SMLA_ERR_UNSUPPORTED;
+  *cluster_ctas = c;
+  *chunk_positions = ch;
+  return SMLA_OK;
+}
+
 extern "C" int sparse_mla_combine(int32_t batch, int32_t num_heads, int32_t nsplit, const float* o_part,
                                   const float* lse_part, void* out, float* lse, smla_stream_t stream) {
   if (batch < 1 || num_heads < 1 || nsplit < 1 || nsplit > kMaxCombineSplit) return SMLA_ERR_INVALID_ARG;
