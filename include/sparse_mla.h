@@ -164,6 +164,34 @@ int sparse_mla_split(const smla_dims* dims, int32_t nsplit, const void* q, const
                      float sm_scale, float* o_part, float* lse_part, uint32_t* err_word,
                      smla_stream_t stream);
 
+/* sparse_mla_decode that also reports the index -> address step (a1) as the
+ * decode itself performed it: rows_out[b][i] (int64, [B][topk], 8-byte
+ * aligned) receives the physical row (page * 64 + slot) whose record the split
+ * kernel's gather warps loaded for top-k entry i of query b, or -1 for an
+ * entry they skipped (rules above).  Every entry is written once per head
+ * group (the same value).  Same launches as sparse_mla_decode, with the extra
+ * stores; meant for checking that the decode gathers exactly the rows the
+ * top-k list names ("Inside the Decode Performance Investigation", Task 1:
+ * scattered FP8 page-gathers).  Returns SMLA_ERR_INVALID_ARG for a null or
+ * misaligned rows_out, else as sparse_mla_decode. */
+int sparse_mla_decode_rows(const smla_dims* dims, const void* q, const void* kv_cache,
+                           const int32_t* block_table, const int32_t* topk_idx,
+                           const int32_t* seq_lens, float sm_scale, void* out, float* lse,
+                           void* workspace, size_t workspace_bytes, int64_t* rows_out,
+                           smla_stream_t stream);
+
+/* Test hook for the split kernel's failure path: every wait of the kernel's
+ * internal pipeline (one thread group waiting for another's shared-memory
+ * tile, an MMA or a bulk copy) gives up after `ns` nanoseconds of the GPU's
+ * global timer, sets SMLA_DEVERR_TIMEOUT and leaves that call's outputs
+ * unwritten; the waits that drain in-flight MMAs and copies before the kernel
+ * exits keep their own limit.  Applies to launches made after the call, from
+ * every host thread.  ns = 0 restores the default (one second).  A limit far
+ * below a tile's latency makes every launch fail: it exists to test that such
+ * a failure is reported and leaves the context usable.  Host only; returns
+ * SMLA_OK. */
+int sparse_mla_debug_set_wait_limit(uint64_t ns);
+
 /* Shapes of one KV append call. */
 typedef struct smla_append_dims {
   int32_t tokens;             /* new tokens to write, >= 0                               */
@@ -285,13 +313,26 @@ const char* sparse_mla_status_string(int status);
  *     sparse_mla_decode with a caller workspace or a smaller nsplit then.
  *   - No cudaMalloc, cudaFree or allocating library call is made.
  *   - Every call shares the array and leaves its contents behind: the error
- *     word is cleared at the start of each call (it is not readable through
- *     this API), and calls that overlap on the GPU (other streams, other
- *     threads) race on the array and must be ordered by the caller. */
+ *     word is cleared at the start of each call and holds that call's
+ *     SMLA_DEVERR_* bits afterwards (sparse_mla_noalloc_read_errors), and
+ *     calls that overlap on the GPU (other streams, other threads) race on the
+ *     array and must be ordered by the caller.
+ *   - Dims are checked as sparse_mla_decode checks them, with the same status
+ *     codes.
+ *   - The device address is cached per device index for the life of the
+ *     process; after cudaDeviceReset the library must not be called again. */
 #define SMLA_NOALLOC_SCRATCH_BYTES (32u << 20)
 int sparse_mla_decode_noalloc(const smla_dims* dims, const void* q, const void* kv_cache,
                               const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
                               float sm_scale, void* out, float* lse, smla_stream_t stream);
+
+/* Copy the device error word of the last sparse_mla_decode_noalloc call on the
+ * current device (SMLA_DEVERR_* bits) to *flags.  Enqueued on `stream`, then
+ * synchronises it (not capturable); order it after that call.  No
+ * allocation.  Returns SMLA_ERR_INVALID_ARG for a null flags, SMLA_ERR_CUDA if
+ * the copy fails.  The pages have no counterpart: it completes the
+ * workspace-free entry point above. */
+int sparse_mla_noalloc_read_errors(uint32_t* flags, smla_stream_t stream);
 
 #ifdef __cplusplus
 }

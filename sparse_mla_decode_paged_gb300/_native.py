@@ -53,6 +53,10 @@ _SIGS = {
     "sparse_mla_read_errors": (C.c_int, [_P, C.POINTER(C.c_uint32), _P]),
     "sparse_mla_status_string": (C.c_char_p, [C.c_int]),
     "sparse_mla_decode_noalloc": (C.c_int, [C.POINTER(SmlaDims), _P, _P, _P, _P, _P, C.c_float, _P, _P, _P]),
+    "sparse_mla_noalloc_read_errors": (C.c_int, [C.POINTER(C.c_uint32), _P]),
+    "sparse_mla_decode_rows": (C.c_int, [C.POINTER(SmlaDims), _P, _P, _P, _P, _P, C.c_float, _P, _P, _P,
+                                         C.c_size_t, _P, _P]),
+    "sparse_mla_debug_set_wait_limit": (C.c_int, [C.c_uint64]),
 }
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_WORKSPACE",

@@ -115,6 +115,37 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
     return out, lse
 
 
+def sparse_mla_decode_rows(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                           topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
+                           workspace: Optional[torch.Tensor] = None, nsplit: int = 0, stream=None,
+                           heads_per_cta: int = 0, rows: Optional[torch.Tensor] = None):
+    """sparse_mla_decode that also returns the rows the decode's split kernel loaded:
+    (out bf16 [B,H,512], lse fp32 [B,H], rows int64 [B,topk], -1 for skipped entries)."""
+    _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
+    B, H = q.shape[0], q.shape[1]
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta)
+    if nsplit == 0:
+        nsplit = plan(dims, q.device.index).nsplit
+        dims.nsplit = nsplit
+    out = torch.empty((B, H, D_LATENT), dtype=torch.bfloat16, device=q.device)
+    lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+    if rows is None:
+        rows = torch.empty(topk_idx.shape, dtype=torch.int64, device=q.device)
+    _need(rows, "rows", torch.int64, 2)
+    if workspace is None:
+        workspace = alloc_workspace(dims, nsplit, q.device)
+    check("sparse_mla_decode_rows", _lib().sparse_mla_decode_rows(
+        C.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens),
+        C.c_float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), C.c_size_t(workspace.numel()),
+        _ptr(rows), _stream(stream)))
+    return out, lse, rows
+
+
+def debug_set_wait_limit(ns: int) -> None:
+    """Time limit of the split kernel's pipeline waits for later launches (0 = the default, 1 s)."""
+    check("sparse_mla_debug_set_wait_limit", _lib().sparse_mla_debug_set_wait_limit(int(ns)))
+
+
 def sparse_mla_split(q, kv_cache, block_table, topk_idx, seq_lens, sm_scale: float, nsplit: int,
                      err_word: Optional[torch.Tensor] = None, stream=None, heads_per_cta: int = 0):
     """Partials: o_part fp32 [B,nsplit,H,512], lse_part fp32 [B,nsplit,H]."""

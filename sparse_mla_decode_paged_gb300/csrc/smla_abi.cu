@@ -4,15 +4,25 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "smla_internal.h"
 
 using namespace smla;
 
 namespace {
 
+std::atomic<uint64_t> g_wait_limit_ns{kDefaultWaitNs};
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int check_dims(const smla_dims* d) {
+}  // namespace
+
+namespace smla {
+
+uint64_t split_wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
+
+int check_decode_dims(const smla_dims* d) {
   if (!d) return SMLA_ERR_INVALID_ARG;
   if (d->batch < 1 || d->topk < 1 || d->max_pages_per_seq < 1 || d->num_pages < 1 || d->nsplit < 0)
     return SMLA_ERR_INVALID_ARG;
@@ -24,6 +34,12 @@ int check_dims(const smla_dims* d) {
   if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
   return SMLA_OK;
 }
+
+}  // namespace smla
+
+namespace {
+
+int check_dims(const smla_dims* d) { return check_decode_dims(d); }
 
 int check_inputs(const void* q, const void* kv, const int32_t* bt, const int32_t* topk, const int32_t* seq) {
   if (!q || !kv || !bt || !topk || !seq) return SMLA_ERR_INVALID_ARG;
@@ -67,7 +83,50 @@ SplitParams make_params(const smla_dims* d, int nsplit, int nh, const void* q, c
   p.nh = nh;
   p.q_per_req = d->queries_per_request > 1 ? d->queries_per_request : 1;
   p.split_len = (d->topk + nsplit - 1) / nsplit;
+  p.wait_ns = split_wait_limit_ns();
   return p;
+}
+
+// The whole decode (split kernel, then the merge when nsplit > 1); rows_out (may be null) receives the
+// row the split kernel's gather warps resolved for every top-k entry.
+int decode_impl(const smla_dims* dims, const void* q, const void* kv_cache, const int32_t* block_table,
+                const int32_t* topk_idx, const int32_t* seq_lens, float sm_scale, void* out, float* lse,
+                void* workspace, size_t workspace_bytes, int64_t* rows_out, cudaStream_t s) {
+  int st = check_dims(dims);
+  if (st != SMLA_OK) return st;
+  st = check_inputs(q, kv_cache, block_table, topk_idx, seq_lens);
+  if (st != SMLA_OK) return st;
+  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return SMLA_ERR_INVALID_ARG;
+  if (rows_out && !aligned(rows_out, 8)) return SMLA_ERR_INVALID_ARG;
+  // a fixed split count fixes the workspace size: checked before the device is queried for the plan
+  if (dims->nsplit > 0) {
+    const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, dims->nsplit);
+    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
+  }
+  smla_plan plan;
+  st = plan_on_current_device(dims, dims->nsplit, &plan);
+  if (st != SMLA_OK) return st;
+  const int nsplit = plan.nsplit;
+  const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, nsplit);
+  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  SplitParams p = make_params(dims, nsplit, plan.heads_per_cta, q, kv_cache, block_table, topk_idx, seq_lens,
+                              sm_scale);
+  p.err = reinterpret_cast<uint32_t*>(ws);
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.rows_out = rows_out;
+  p.final_out = (nsplit == 1);
+  if (nsplit > 1) {
+    const size_t lse_bytes = ((size_t)dims->batch * nsplit * dims->num_heads * sizeof(float) + 255) / 256 * 256;
+    p.lse_part = reinterpret_cast<float*>(ws + kWorkspaceHeader);
+    p.o_part = reinterpret_cast<float*>(ws + kWorkspaceHeader + lse_bytes);
+  }
+  if (launch_split(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (nsplit > 1 &&
+      launch_combine(dims->batch, dims->num_heads, nsplit, p.o_part, p.lse_part, p.out, lse, s) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return SMLA_OK;
 }
 
 }  // namespace
@@ -107,39 +166,21 @@ extern "C" int sparse_mla_decode(const smla_dims* dims, const void* q, const voi
                                  const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
                                  float sm_scale, void* out, float* lse, void* workspace, size_t workspace_bytes,
                                  smla_stream_t stream) {
-  int st = check_dims(dims);
-  if (st != SMLA_OK) return st;
-  st = check_inputs(q, kv_cache, block_table, topk_idx, seq_lens);
-  if (st != SMLA_OK) return st;
-  if (!out || !lse || !aligned(out, 16) || !aligned(lse, 4)) return SMLA_ERR_INVALID_ARG;
-  // a fixed split count fixes the workspace size: checked before the device is queried for the plan
-  if (dims->nsplit > 0) {
-    const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, dims->nsplit);
-    if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
-  }
-  smla_plan plan;
-  st = plan_on_current_device(dims, dims->nsplit, &plan);
-  if (st != SMLA_OK) return st;
-  const int nsplit = plan.nsplit;
-  const size_t need = workspace_bytes_for(dims->batch, dims->num_heads, nsplit);
-  if (!workspace || workspace_bytes < need || !aligned(workspace, 256)) return SMLA_ERR_WORKSPACE;
-  unsigned char* ws = static_cast<unsigned char*>(workspace);
-  SplitParams p = make_params(dims, nsplit, plan.heads_per_cta, q, kv_cache, block_table, topk_idx, seq_lens,
-                              sm_scale);
-  p.err = reinterpret_cast<uint32_t*>(ws);
-  p.out = static_cast<uint16_t*>(out);
-  p.lse = lse;
-  p.final_out = (nsplit == 1);
-  if (nsplit > 1) {
-    const size_t lse_bytes = ((size_t)dims->batch * nsplit * dims->num_heads * sizeof(float) + 255) / 256 * 256;
-    p.lse_part = reinterpret_cast<float*>(ws + kWorkspaceHeader);
-    p.o_part = reinterpret_cast<float*>(ws + kWorkspaceHeader + lse_bytes);
-  }
-  cudaStream_t s = (cudaStream_t)stream;
-  if (launch_split(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  if (nsplit > 1 &&
-      launch_combine(dims->batch, dims->num_heads, nsplit, p.o_part, p.lse_part, p.out, lse, s) != cudaSuccess)
-    return SMLA_ERR_CUDA;
+  return decode_impl(dims, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+                     workspace_bytes, nullptr, (cudaStream_t)stream);
+}
+
+extern "C" int sparse_mla_decode_rows(const smla_dims* dims, const void* q, const void* kv_cache,
+                                      const int32_t* block_table, const int32_t* topk_idx, const int32_t* seq_lens,
+                                      float sm_scale, void* out, float* lse, void* workspace,
+                                      size_t workspace_bytes, int64_t* rows_out, smla_stream_t stream) {
+  if (!rows_out) return SMLA_ERR_INVALID_ARG;
+  return decode_impl(dims, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale, out, lse, workspace,
+                     workspace_bytes, rows_out, (cudaStream_t)stream);
+}
+
+extern "C" int sparse_mla_debug_set_wait_limit(uint64_t ns) {
+  g_wait_limit_ns.store(ns ? ns : kDefaultWaitNs, std::memory_order_relaxed);
   return SMLA_OK;
 }
 

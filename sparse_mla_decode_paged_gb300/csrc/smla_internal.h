@@ -38,7 +38,17 @@ struct SplitParams {
   float* o_part;              // [B][nsplit][H][512]
   float* lse_part;            // [B][nsplit][H]
   uint32_t* err;              // device error word (may be null)
+  int64_t* rows_out;          // [B][topk] or null: the row the gather warps resolved for each entry
+  uint64_t wait_ns;           // time limit of each pipeline wait inside the kernel
 };
+
+// Host checks of a decode's dims (status code; SMLA_OK when the split kernel supports them).
+int check_decode_dims(const smla_dims* d);
+
+// Time limit of the split kernel's pipeline waits: kDefaultWaitNs unless a test set another one
+// (sparse_mla_debug_set_wait_limit).
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;
+uint64_t split_wait_limit_ns();
 
 // Everything the KV append kernel needs for one launch.
 struct AppendParams {

@@ -25,6 +25,7 @@ namespace smla {
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = 32u << 20;   // 32 MiB
+static_assert(kNoAllocScratchBytes == SMLA_NOALLOC_SCRATCH_BYTES, "the header states the scratch size");
 constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
@@ -55,7 +56,9 @@ extern "C" int sparse_mla_decode_noalloc(const smla_dims* dims, const void* q, c
                                          const int32_t* block_table, const int32_t* topk_idx,
                                          const int32_t* seq_lens, float sm_scale, void* out, float* lse,
                                          smla_stream_t stream) {
-  if (!dims) return SMLA_ERR_INVALID_ARG;
+  // the same dims checks (and status codes) as sparse_mla_decode, before any size is computed
+  const int dst = check_decode_dims(dims);
+  if (dst != SMLA_OK) return dst;
   // the split count decides the scratch size; fix it here so the size check and the call agree
   smla_dims d = *dims;
   if (d.nsplit == 0) {
@@ -77,4 +80,15 @@ extern "C" int sparse_mla_decode_noalloc(const smla_dims* dims, const void* q, c
   if (cudaMemsetAsync(scratch, 0, sizeof(uint32_t), (cudaStream_t)stream) != cudaSuccess) return SMLA_ERR_CUDA;
   return sparse_mla_decode(&d, q, kv_cache, block_table, topk_idx, seq_lens, sm_scale, out, lse, scratch,
                            kNoAllocScratchBytes, stream);
+}
+
+extern "C" int sparse_mla_noalloc_read_errors(uint32_t* flags, smla_stream_t stream) {
+  if (!flags) return SMLA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int st = scratch_of_current_device(&scratch);
+  if (st != SMLA_OK) return st;
+  // the error word is the array's first 4 bytes (the workspace header of the last call)
+  if (cudaMemcpyAsync(flags, scratch, sizeof(uint32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream) != cudaSuccess)
+    return SMLA_ERR_CUDA;
+  return cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }

@@ -42,15 +42,30 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// Non-blocking test of the phase with the given parity (try_wait instead may suspend the thread until
+// the phase completes or a hardware time limit passes).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Limits below this are served by polling with test_wait and reading the clock at every poll, so that
+// they hold however long a try_wait would suspend (used to exercise the give-up path).
+constexpr uint64_t kShortWaitNs = 100000ull;
+
 // Wait until the phase with the given parity completes.  Gives up after
 // `limit_ns` or as soon as *abort is set; returns false then (and sets *abort).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                   uint64_t limit_ns = 1000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+  if (limit_ns < kShortWaitNs) {
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+      if (mbar_test_wait(bar, parity)) return true;
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
@@ -58,28 +73,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
       }
     }
   }
-}
-
-// Acquire at cluster scope: for barriers that another CTA of the cluster arrives on after
-// writing into this CTA's shared memory.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait_bounded with cluster-scope acquire.
-__device__ __forceinline__ bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                                          uint64_t limit_ns = 1000000000ull) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 0) {
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
@@ -116,19 +113,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
-}
-
-__device__ __forceinline__ void st_cluster128(uint32_t caddr, uint4 v) {
-  asm volatile("st.shared::cluster.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(caddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// Arrive, with release semantics at cluster scope, on an mbarrier given by its shared::cluster address
-// (possibly in another CTA of the cluster).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
 // Every thread of every CTA of the cluster (non-aligned forms).
@@ -202,17 +186,6 @@ __device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc], kind::f16.  A is M=128 rows (TMEM lanes) x K=16 fp16
-// packed two per 32-bit column (8 columns, element 2c in the low half of column c).
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
 // One lane of a converged warp (the lowest active lane): MMAs issued this way from warp-uniform code
 // leave their operands in uniform registers, which issues faster than a single-thread branch.
 __device__ __forceinline__ bool elect_one() {
@@ -225,16 +198,6 @@ __device__ __forceinline__ bool elect_one() {
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same shared-memory offset in every CTA of
-// `cta_mask` (cluster ranks as bits).
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
 }
 
 #define SMLA_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
@@ -258,7 +221,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       SMLA_W8(0), SMLA_W8(8), SMLA_W8(16), SMLA_W8(24));
 }
 
-// 32 lanes x 16 consecutive 32-bit columns (store).
 // 32 lanes x 16 consecutive 32-bit columns (load).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
@@ -266,16 +228,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
                : "r"(taddr));
 }
 
+// 32 lanes x 16 consecutive 32-bit columns (store).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
           taddr),
       SMLA_W8(0), SMLA_W8(8));
-}
-
-// 32 lanes x 8 consecutive 32-bit columns (store).
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), SMLA_W8(0));
 }
 
 #undef SMLA_R8
@@ -293,13 +251,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
   return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
-// As sw128_desc with the 64-byte swizzle (value 4 at bits 61..63): K-major rows of 64 B, 8-row
-// groups of 512 B (SBO), 16-byte units XOR-ed with bits 1..2 of the row.
-__device__ __forceinline__ uint64_t sw64_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (4ull << 61);
 }
 
 // As sw128_desc for a swizzle span of 128, 64 or 32 bytes (layout type 2, 4 or 6 at bits 61..63).
@@ -336,8 +287,6 @@ __device__ __forceinline__ int ldg_i32_now(const int32_t* p) {
   return v;
 }
 
-// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 (TMA engine; no
-// registers or L1 space are used and nothing waits for it).
 // Programmatic dependent launch: a grid launched with programmatic stream serialization after this
 // one may start once every CTA here has signalled (or exited); it waits for this grid's completion
 // and memory with griddep_wait before touching its results.
@@ -351,18 +300,11 @@ __device__ __forceinline__ void prefetch_l2_line(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p) : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16, 16-byte aligned) of global memory into L2 (TMA engine; no
+// registers or L1 space are used and nothing waits for it).
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
-
-// Bulk copy shared -> global (TMA engine), tracked by the issuing thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 
 // 2^x, hardware approximation (relative error about 2^-22), flushing subnormal results to zero.
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -381,18 +323,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
 // copy) reads after a proxy fence and a thread barrier, so no C++ access needs ordering against it.
 __device__ __forceinline__ void sts128_async_only(uint32_t saddr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(saddr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w));
-}
-
-__device__ __forceinline__ void sts16(uint32_t saddr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(v));
-}
-
-__device__ __forceinline__ void sts32(uint32_t saddr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(saddr), "r"(v));
-}
-
-__device__ __forceinline__ void sts64(uint32_t saddr, uint32_t a, uint32_t b) {
-  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(saddr), "r"(a), "r"(b));
 }
 
 __device__ __forceinline__ void sts128(uint32_t saddr, uint4 v) {

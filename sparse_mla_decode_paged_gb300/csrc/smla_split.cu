@@ -42,13 +42,16 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "smla_device.cuh"
 #include "smla_ptx.cuh"
+#include "smla_split_layout.cuh"
 
 namespace smla {
 namespace {
 
-constexpr int kTile = 128;
 constexpr int kHeadsMax = 64;
 constexpr int kThreads = 384;
 constexpr int kSoftWarps = 4;
@@ -59,37 +62,12 @@ constexpr float kRescaleThreshold = 8.0f;         // log2 units: P <= 2^8
 constexpr float kFp16Max = 65504.0f;
 constexpr float kMaxScale = 16384.0f;             // P * mant <= 2^8 * 2^7 stays inside fp16
 
-constexpr uint32_t kKChunk = kTile * 128;         // 128 tokens x 64 dims fp16
-constexpr uint32_t kKBytes = 9 * kKChunk;         // 147456
-constexpr uint32_t kRopeChunk = 8;
 // Before tile 0 is converted the K tile is idle: it receives the raw bf16 Q of the head group (up to
 // 64 x 1152 bytes at offset 0) and tile 0's raw E4M3 codes (128 x 512 bytes) by bulk copy.
 constexpr uint32_t kRawQMax = kHeadsMax * kDQK * 2;          // 73728
 constexpr uint32_t kRawLatOff = kRawQMax;
 static_assert(kRawLatOff + kTile * kDLatent <= kKBytes, "raw staging inside the K tile");
 constexpr uint32_t kGatherBar = 4;                           // named barrier of the gather warps
-
-// Per head-group size NH: Q chunks of NH rows x 64 dims, TMEM columns, MMA N, and the P * mant
-// buffers ([128 tokens][NH heads] fp16, MN-major with NH * 2-byte rows: a 128-, 64- or 32-byte
-// swizzle span).
-template <int NH>
-struct Cfg {
-  static_assert(NH == 16 || NH == 32 || NH == 64, "heads per CTA");
-  static constexpr uint32_t kQChunk = NH * 128;
-  static constexpr uint32_t kQBytes = 9 * kQChunk;
-  static constexpr uint32_t kKBase = kQBytes;               // a multiple of 1024
-  static constexpr uint32_t kMiscOff = kKBase + kKBytes;
-  static constexpr uint32_t kTmemCols = 8 * NH;             // 128, 256, 512
-  static constexpr uint32_t kSCol = 4 * NH;                 // score buffer b at 4 NH + NH b
-  static constexpr uint32_t kIdescQK = ptx::idesc_f16(128, NH, 0, 0);
-  static constexpr uint32_t kIdescPV = ptx::idesc_f16(128, NH, 1, 1);
-  static constexpr int kPRow = 2 * NH;                      // bytes of one token's P * mant row
-  static constexpr int kPUnits = NH / 8;                    // 16-byte units per row
-  static constexpr uint32_t kPStep = 16 * kPRow;            // bytes of 16 tokens (one PV MMA's K)
-  static constexpr int kR = NH >= 32 ? NH / 32 : 1;         // heads per lane after a reduce-scatter
-  static constexpr int kChunkCols = NH >= 32 ? 32 : 16;     // TMEM columns per O^T chunk
-  static constexpr int kChunks = 4 * NH / kChunkCols;       // O^T chunks
-};
 
 struct Misc {
   uint64_t q_raw;            // raw Q landed in the K tile (bulk copy)
@@ -117,47 +95,6 @@ struct Misc {
 template <int NH>
 constexpr size_t smem_bytes() { return 1024 + Cfg<NH>::kMiscOff + sizeof(Misc); }
 static_assert(smem_bytes<64>() <= 232448, "shared memory per CTA");
-
-// Byte offset of 16-byte unit u of row r in a buffer of `row_bytes`-wide rows with the matching
-// swizzle (128, 64 or 32 bytes): the unit index is XOR-ed with the row's bits above the span.
-template <int kRowBytes>
-__device__ __forceinline__ uint32_t swz_row(uint32_t row, uint32_t unit) {
-  constexpr uint32_t mask = kRowBytes / 16 - 1;
-  constexpr int shift = kRowBytes == 128 ? 0 : kRowBytes == 64 ? 1 : 2;
-  return row * kRowBytes + ((unit ^ ((row >> shift) & mask)) << 4);
-}
-
-__device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t unit) {
-  return row * 128u + ((unit ^ (row & 7u)) << 4);
-}
-
-// MMA issue.  A descriptor's start address sits in its low 14 bits in 16-byte units, so the operand
-// at byte offset o from a base is the base descriptor + o / 16 (shared addresses stay below 256 KB:
-// no carry).  The issuers are unrolled with compile-time offsets: one thread issues every MMA, and
-// rebuilding each descriptor on that thread costs more than the MMA itself.
-//
-// QK of chunks [ch0, ch0 + nch) into one score buffer.
-template <int NH, int kCh0, int kNch, bool kAccumulate = false>
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint64_t dK, uint64_t dQ) {
-#pragma unroll
-  for (int cc = 0; cc < kNch; ++cc)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      ptx::mma_f16_ss(d_tmem, dK + (uint64_t)(((kCh0 + cc) * kKChunk + 32 * kk) >> 4),
-                      dQ + (uint64_t)(((kCh0 + cc) * Cfg<NH>::kQChunk + 32 * kk) >> 4), Cfg<NH>::kIdescQK,
-                      (kAccumulate || cc != 0 || kk != 0) ? 1u : 0u);
-}
-
-// PV of latent block kB: O^T_b (+)= K'_b^T . (P * mant_b); A is the K tile read MN-major (dims of
-// chunks 2b, 2b + 1), B the 16-token slices of the P * mant buffer.
-template <int NH, int kB>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint64_t dV, uint64_t dBuf, bool accumulate) {
-#pragma unroll
-  for (int kk = 0; kk < kTile / 16; ++kk)
-    ptx::mma_f16_ss(tmem + NH * kB, dV + (uint64_t)((2 * kB * kKChunk + kk * 2048) >> 4),
-                    dBuf + (uint64_t)((kk * Cfg<NH>::kPStep) >> 4), Cfg<NH>::kIdescPV,
-                    (accumulate || kk > 0) ? 1u : 0u);
-}
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
@@ -309,17 +246,17 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     const int pos = x.pos0 + j * kTile + tl;
     return (j < x.n_tiles && pos < x.pos_end) ? ptx::ldg_i32_now(tk_row + pos) : -1;
   };
-  auto page_load = [&](int t) -> int {      // block-table entry of t, or 0 when t is not looked up
-    const bool used = t >= 0 && t < seq_len && (t >> 6) < p.max_pages;
-    return used ? ptx::ldg_i32_now(bt_row + (t >> 6)) : 0;
+  auto page_load = [&](int t) -> int {      // block-table entry of t (load issued here), or 0 when t reads none
+    return entry_reads_table(t, seq_len, p.max_pages) ? ptx::ldg_i32_now(bt_row + (t >> 6)) : 0;
   };
   auto row_from = [&](int t, int page) -> int64_t {
-    if (t < 0 || t >= seq_len) return -1;
-    if ((t >> 6) >= p.max_pages || page < 0 || (int64_t)page >= p.num_pages) {
-      if (p.err) atomicOr(p.err, SMLA_DEVERR_PAGE_RANGE);
-      return -1;
-    }
-    return (int64_t)page * kPageSize + (t & (kPageSize - 1));
+    return row_from_page(t, page, seq_len, p.max_pages, p.num_pages, p.err);
+  };
+  // the row this lane resolved for its entry of tile j (the row whose record the tile loads), written
+  // out when the caller asked for the resolved rows
+  auto record_row = [&](int j, int64_t r) {
+    const int pos = x.pos0 + j * kTile + tl;
+    if (p.rows_out && lane < 16 && j < x.n_tiles && pos < x.pos_end) p.rows_out[(size_t)x.b * p.topk_n + pos] = r;
   };
 
   // Record bytes of the warp's 16 tokens: load k reads token 16 gw + k's 512 code bytes (one
@@ -357,6 +294,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   const int pg0 = page_load(t0);
   int pg1 = page_load(t1), pg2 = page_load(t2);
   int64_t row = row_from(t0, pg0);
+  record_row(0, row);
   // tile 0's codes by bulk copy into the idle K tile (register loads are bound by the loads an SM
   // keeps in flight, which a cold first tile feels most); its rope and scales by register loads.  No
   // L2 prefetch of tile 0: the bulk copies fetch its lines.
@@ -378,11 +316,11 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
   for (int i = 0; i < x.n_tiles; ++i) {
     const bool valid = row >= 0;
     // the K tile is free once every PV MMA of the previous tile is done
-    if (i > 0) ok = ptx::mbar_wait_warp(&ms.pv_done, (i - 1) & 1, x.abort, lane) && ok;
+    if (i > 0) ok = ptx::mbar_wait_warp(&ms.pv_done, (i - 1) & 1, x.abort, lane, p.wait_ns) && ok;
     if (i == 0) {
       // tile 0's codes from the raw copy into registers; the K tile is written only once every gather
       // warp has read its codes and every softmax warp its raw Q
-      ok = ptx::mbar_wait_warp(&ms.raw0, 0, x.abort, lane) && ok;
+      ok = ptx::mbar_wait_warp(&ms.raw0, 0, x.abort, lane, p.wait_ns) && ok;
 #pragma unroll
       for (int k = 0; k < 16; ++k) {
         const int64_t rk = shfl_i64(row, k);
@@ -390,7 +328,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
                                  : make_uint4(0, 0, 0, 0);
       }
       ptx::named_bar_sync(kGatherBar, kGatherWarps * 32);
-      ok = ptx::mbar_wait_warp(&ms.k_free0, 0, x.abort, lane) && ok;
+      ok = ptx::mbar_wait_warp(&ms.k_free0, 0, x.abort, lane, p.wait_ns) && ok;
     }
     if (ok) {
       const float s4[4] = {__uint_as_float(sc.x), __uint_as_float(sc.y), __uint_as_float(sc.z),
@@ -444,6 +382,7 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     if (lane == 0) ptx::mbar_arrive(&ms.tile_full);
     // tile i + 1's records, tile i + 3's into L2, tile i + 4's pages, tile i + 5's entries
     row = row_from(t1, pg1);
+    record_row(i + 1, row);
     if (i + 1 < x.n_tiles) load_tile(row);
     if (i + 3 < x.n_tiles) prefetch_row(row_from(t3, pg3));
     t1 = t2; pg1 = pg2;
@@ -471,7 +410,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   {
     // Q head group -> fp16, 128B-swizzled, zero rows past the valid heads: NH rows x 72 16-byte units,
     // read from the raw bf16 rows the bulk copy put at the start of the K tile (unit id at 16 id)
-    ok = ptx::mbar_wait_warp(&ms.q_raw, 0, x.abort, lane) && ok;
+    ok = ptx::mbar_wait_warp(&ms.q_raw, 0, x.abort, lane, p.wait_ns) && ok;
     constexpr int kUnits = NH * 72 / kSoftThreads;   // per thread: 9, 18 or 36
     constexpr int kBatch = kUnits < 18 ? kUnits : 18;
 #pragma unroll 1
@@ -485,7 +424,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 #pragma unroll
       for (int k = 0; k < kBatch; ++k) {
         const int id = t + kSoftThreads * (k0 + k), n = id / 72, j = id % 72;
-        ptx::sts128_async_only(x.q_base + (j >> 3) * C::kQChunk + swz128(n, j & 7), bf8_to_h8(v[k], range_bad));
+        ptx::sts128_async_only(x.q_base + chunked_offset(C::kQChunk, n, j), bf8_to_h8(v[k], range_bad));
       }
     }
     ptx::fence_proxy_async_smem();
@@ -501,17 +440,13 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 #pragma unroll
   for (int r = 0; r < R; ++r) lsum[r] = 0.f;
   const uint32_t bufR = x.k_base + kRopeChunk * kKChunk, buf0 = x.k_base, buf1 = x.k_base + kKChunk;
-  const uint64_t dK = ptx::sw128_desc(x.k_base, 16, 1024), dQ = ptx::sw128_desc(x.q_base, 16, 1024);
-  const uint64_t dV = ptx::sw128_desc(x.k_base, kKChunk, 1024);   // K tile as the MN-major A of PV
-  // P * mant buffers as MN-major B: one NH-head swizzle span along N (the leading offset is never
-  // stepped), 8-token groups 8 * row bytes apart
-  const uint64_t dBufR = ptx::swz_desc(bufR, 8 * C::kPRow, 8 * C::kPRow, C::kPRow),
-                 dBuf0 = ptx::swz_desc(buf0, 8 * C::kPRow, 8 * C::kPRow, C::kPRow),
-                 dBuf1 = ptx::swz_desc(buf1, 8 * C::kPRow, 8 * C::kPRow, C::kPRow);
+  const uint64_t dK = desc_qk_operand(x.k_base), dQ = desc_qk_operand(x.q_base);
+  const uint64_t dV = desc_v(x.k_base);      // K tile as the MN-major A of PV
+  const uint64_t dBufR = desc_pm<NH>(bufR), dBuf0 = desc_pm<NH>(buf0), dBuf1 = desc_pm<NH>(buf1);
 
   for (int i = 0; i < x.n_tiles; ++i) {
     const uint32_t ph = i & 1;
-    ok = ptx::mbar_wait_warp(&ms.tile_full, ph, x.abort, lane) && ok;
+    ok = ptx::mbar_wait_warp(&ms.tile_full, ph, x.abort, lane, p.wait_ns) && ok;
     const bool valid = ms.valid[t];
     float mant[4];
 #pragma unroll
@@ -519,7 +454,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     // QK of latent block b into score buffer b, the rope (stored as rope / mant_0) into buffer 0
     // after block 0; all 36 MMAs in one batch
     if (issue_warp) {
-      if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane);
+      if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane, p.wait_ns);
       mma_ok = mma_ok && ok;
       if (mma_ok) {
         ptx::tc_fence_after();
@@ -544,7 +479,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
     // scores s = sum_b mant_b S_b (the rope is inside S_0), buffers in the order they complete
 #pragma unroll 1
     for (int bb = 0; bb < 4; ++bb) {
-      ok = ptx::mbar_wait_warp(&ms.s_full[bb], ph, x.abort, lane) && ok;
+      ok = ptx::mbar_wait_warp(&ms.s_full[bb], ph, x.abort, lane, p.wait_ns) && ok;
       if (ok) {
         ptx::tc_fence_after();
         const float f = c2 * (bb == 0 ? mant[0] : bb == 1 ? mant[1] : bb == 2 ? mant[2] : mant[3]);
@@ -679,7 +614,7 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 #pragma unroll
       for (int r = 0; r < R; ++r) lsum[r] += ps[r];
     }
-    ok = ptx::mbar_wait_warp(&ms.pv0_done, ph, x.abort, lane) && ok;
+    ok = ptx::mbar_wait_warp(&ms.pv0_done, ph, x.abort, lane, p.wait_ns) && ok;
     write_pm(1, buf0);
     write_pm(2, bufR);
     write_pm(3, buf1);
@@ -836,7 +771,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   else softmax_role<NH>(x, warp, lane);
 
   // ------------------------------------------------------------------ epilogue
-  bool ok = ptx::mbar_wait_warp(&ms.pv_done, (x.n_tiles - 1) & 1, x.abort, lane);
+  bool ok = ptx::mbar_wait_warp(&ms.pv_done, (x.n_tiles - 1) & 1, x.abort, lane, p.wait_ns);
   ptx::tc_fence_after();
   __syncthreads();                           // row sums of the softmax warps are in ms.red
   if (threadIdx.x < NH) {
@@ -896,25 +831,39 @@ int split_ctas_per_sm(int H) {
 
 namespace {
 
+constexpr int kMaxDevices = 64;
+
+// Kernel attributes of split_kernel<NH> on the current device: set once per device (a per-device flag,
+// read without a lock once set; the first call on a device configures it under the lock).
+template <int NH>
+cudaError_t configure_split_nh(int dev) {
+  static std::atomic<bool> configured[kMaxDevices];
+  static std::mutex mu;
+  if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e =
+      cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
+  if (e != cudaSuccess) return e;
+  // the smallest shared-memory carveout that holds the CTA: the rest of the SM's SRAM is L1, where the
+  // record loads in flight land (about 28 KB at 64 heads per CTA, 60 KB at 16 or 32)
+  int max_smem = 0;
+  e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+  if (e != cudaSuccess) return e;
+  const int pct = (int)((100 * (smem_bytes<NH>() + 1024) + max_smem - 1) / max_smem);
+  e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributePreferredSharedMemoryCarveout, pct < 100 ? pct : 100);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
+
 template <int NH>
 cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
-  static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
-    if (e != cudaSuccess) return e;
-    // the smallest shared-memory carveout that holds the CTA: the rest of the SM's SRAM is L1, where the
-    // record loads in flight land (about 28 KB at 64 heads per CTA, 60 KB at 16 or 32)
-    int max_smem = 0;
-    e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-    if (e != cudaSuccess) return e;
-    const int pct = (int)((100 * (smem_bytes<NH>() + 1024) + max_smem - 1) / max_smem);
-    e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributePreferredSharedMemoryCarveout, pct < 100 ? pct : 100);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  e = configure_split_nh<NH>(dev);
+  if (e != cudaSuccess) return e;
   const int head_groups = (p.H + NH - 1) / NH;
   dim3 grid(p.nsplit, head_groups, p.B);
   // programmatic stream serialization: the CTAs may be scheduled, and set up, while the previous

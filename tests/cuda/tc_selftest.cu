@@ -1,54 +1,79 @@
-// Self-test of the tcgen05 building blocks used by the split kernel, laid out
-// exactly as the kernel lays them out (64 heads per CTA):
-//   - 128B-swizzled shared-memory fill of the K tile (128 rows x 9 chunks of
-//     64 fp16) and of Q (64 rows x 9 chunks);
-//   - QK: S^T[128 x 64] = A[128 x 576] . Q[64 x 576]^T, K-major smem A and B,
-//     M=128 N=64 (TMEM cols 256..319);
-//   - correction: S^T += L[128 x 512] . Q[:, 0:512]^T with L taken from TMEM
-//     (cols 320..447) in two passes of 256 dims, each written by tcgen05.st;
-//   - PV: O^T[512 x 64] = A[:, 0:512]^T . P, A read MN-major from the same
-//     tile, P MN-major over the rope chunk (TMEM cols 0..255);
-//   - TMEM 32x32b loads and stores.
-// Shared memory is allocated at its maximum so that any misread stays inside it.
+// Self-test of the split kernel's tcgen05 building blocks, using the kernel's own layout header
+// (smla_split_layout.cuh: swizzled offsets, matrix descriptors, MMA issuers), for 16, 32 and 64
+// heads per CTA:
+//   - the K tile (128 tokens x 9 chunks of 64 fp16 dims) and Q (NH rows x 9 chunks), 128B-swizzled;
+//   - QK as the kernel issues it: latent block b (chunks 2b, 2b + 1) into score buffer b, the rope
+//     chunk accumulated into buffer 0 (S^T[128 x NH], TMEM columns 4 NH + NH b);
+//   - PV as the kernel issues it: block 0 with its P * mant operand in the rope chunk, then blocks
+//     1..3 with their operands in chunks 0, rope and 1 (written after block 0's PV completed), each
+//     O^T_b[128 x NH] = K'_b^T . Pm_b with the K tile read MN-major and Pm MN-major with an NH * 2-byte
+//     swizzle span (128, 64 or 32 bytes);
+//   - TMEM 32x32b loads of 16 and 32 columns.
+// Every wait is bounded (1 s of the global timer); a timeout sets *status and skips the rest.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "smla_ptx.cuh"
+#include "smla_split_layout.cuh"
 
 using namespace smla;
 
 namespace {
 
-constexpr int kHeads = 64;
-constexpr int kQChunk = kHeads * 128, kKChunk = 128 * 128;
+template <int NH>
+constexpr size_t selftest_smem() { return 1024 + Cfg<NH>::kQBytes + kKBytes; }
 
-__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t unit) { return row * 128u + ((unit ^ (row & 7u)) << 4); }
+// Each thread reads its TMEM lane (token or dim) of `cols` consecutive columns from `col0` into dst.
+template <int NH>
+__device__ void read_cols(uint32_t tmem, uint32_t col0, int cols, float* dst) {
+  const int warp = threadIdx.x >> 5;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  for (int c = 0; c < cols; c += (NH == 16 ? 16 : 32)) {
+    if constexpr (NH == 16) {
+      uint32_t r[16];
+      ptx::tmem_ld16(tmem + lane_base + col0 + c, r);
+      ptx::tmem_wait_ld();
+      for (int h = 0; h < 16; ++h) dst[c + h] = __uint_as_float(r[h]);
+    } else {
+      uint32_t r[32];
+      ptx::tmem_ld32(tmem + lane_base + col0 + c, r);
+      ptx::tmem_wait_ld();
+      for (int h = 0; h < 32; ++h) dst[c + h] = __uint_as_float(r[h]);
+    }
+  }
+}
 
-__global__ void __launch_bounds__(128, 1) selftest_kernel(const uint16_t* A, const uint16_t* Q, const uint16_t* L,
-                                                           const uint16_t* P, float* S_out, float* O_out,
-                                                           int* status) {
+// Pm [128 tokens][NH] (fp16, row-major) into a P * mant buffer as the kernel lays it out.
+template <int NH>
+__device__ void write_pm(uint32_t buf, const uint16_t* pm) {
+  using C = Cfg<NH>;
+  const int t = threadIdx.x;
+  for (int u = 0; u < C::kPUnits; ++u)
+    ptx::sts128(buf + swz_row<C::kPRow>(t, u), reinterpret_cast<const uint4*>(pm + t * NH)[u]);
+}
+
+template <int NH>
+__global__ void __launch_bounds__(128, 1) selftest_kernel(const uint16_t* K, const uint16_t* Q, const uint16_t* Pm,
+                                                           float* S_out, float* O_out, int* status) {
+  using C = Cfg<NH>;
   extern __shared__ unsigned char raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
-  const uint32_t q_base = ptx::smem_u32(base), k_base = q_base + 9 * kQChunk;
-  __shared__ uint64_t bar[4];
+  const uint32_t q_base = ptx::smem_u32(base), k_base = q_base + C::kKBase;
+  __shared__ uint64_t bar[6];
   __shared__ uint32_t slot;
   __shared__ int abort_flag;
   const int t = threadIdx.x, warp = t >> 5;
-  for (int id = t; id < 128 * 72; id += 128) {
-    const int r = id / 72, j = id % 72;
-    ptx::sts128(k_base + (j >> 3) * kKChunk + swz(r, j & 7), reinterpret_cast<const uint4*>(A)[id]);
-  }
-  for (int id = t; id < kHeads * 72; id += 128) {
-    const int r = id / 72, j = id % 72;
-    ptx::sts128(q_base + (j >> 3) * kQChunk + swz(r, j & 7), reinterpret_cast<const uint4*>(Q)[id]);
-  }
+  for (int id = t; id < 128 * 72; id += 128)
+    ptx::sts128(k_base + chunked_offset(kKChunk, id / 72, id % 72), reinterpret_cast<const uint4*>(K)[id]);
+  for (int id = t; id < NH * 72; id += 128)
+    ptx::sts128(q_base + chunked_offset(C::kQChunk, id / 72, id % 72), reinterpret_cast<const uint4*>(Q)[id]);
   if (t == 0) {
-    for (int i = 0; i < 4; ++i) ptx::mbar_init(&bar[i], 1);
+    for (int i = 0; i < 6; ++i) ptx::mbar_init(&bar[i], 1);
     abort_flag = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 0) {
-    ptx::tmem_alloc(&slot, 512);
+    ptx::tmem_alloc(&slot, C::kTmemCols);
     ptx::tmem_relinquish();
   }
   ptx::fence_proxy_async_smem();
@@ -56,89 +81,106 @@ __global__ void __launch_bounds__(128, 1) selftest_kernel(const uint16_t* A, con
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = slot;
-  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-  const uint32_t idesc_qk = ptx::idesc_f16(128, kHeads, 0, 0);
+  const uint64_t dK = desc_qk_operand(k_base), dQ = desc_qk_operand(q_base), dV = desc_v(k_base);
+  const uint32_t bufR = k_base + kRopeChunk * kKChunk, buf0 = k_base, buf1 = k_base + kKChunk;
+
+  // QK exactly as the kernel issues it
+  if (warp == 0) {
+    if (ptx::elect_one()) {
+      issue_qk<NH, 0, 2>(tmem + C::kSCol, dK, dQ);
+      issue_qk<NH, kRopeChunk, 1, true>(tmem + C::kSCol, dK, dQ);
+      ptx::mma_commit(&bar[0]);
+      issue_qk<NH, 2, 2>(tmem + C::kSCol + NH, dK, dQ);
+      ptx::mma_commit(&bar[1]);
+      issue_qk<NH, 4, 2>(tmem + C::kSCol + 2 * NH, dK, dQ);
+      ptx::mma_commit(&bar[2]);
+      issue_qk<NH, 6, 2>(tmem + C::kSCol + 3 * NH, dK, dQ);
+      ptx::mma_commit(&bar[3]);
+    }
+    __syncwarp();
+  }
   bool ok = true;
-  // QK from shared memory
-  if (t == 0) {
-    for (int c = 0; c < 9; ++c)
-      for (int kk = 0; kk < 4; ++kk)
-        ptx::mma_f16_ss(tmem + 256, ptx::sw128_desc(k_base + c * kKChunk + kk * 32, 16, 1024),
-                        ptx::sw128_desc(q_base + c * kQChunk + kk * 32, 16, 1024), idesc_qk, (c | kk) != 0);
-  }
-  // correction from TMEM, two passes of 256 dims
-  for (int pass = 0; pass < 2 && ok; ++pass) {
-    if (pass == 1) {
-      ok = ptx::mbar_wait_bounded(&bar[0], 0, &abort_flag);   // pass 0 MMAs done: TMEM L may be overwritten
-      ptx::tc_fence_after();
-    }
-    for (int cb = 0; cb < 8; ++cb) {   // 8 x 16 columns = 256 fp16 of row t
-      uint32_t r[16];
-      for (int q = 0; q < 16; ++q) {
-        const int d = pass * 256 + cb * 32 + 2 * q;
-        r[q] = (uint32_t)L[t * 512 + d] | ((uint32_t)L[t * 512 + d + 1] << 16);
-      }
-      ptx::tmem_st16(tmem + lane_base + 320 + 16 * cb, r);
-    }
-    ptx::tmem_wait_st();
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    if (t == 0) {
-      for (int kk = 0; kk < 16; ++kk) {
-        const int c = pass * 4 + (kk >> 2);
-        ptx::mma_f16_ts(tmem + 256, tmem + 320 + 8 * kk,
-                        ptx::sw128_desc(q_base + c * kQChunk + (kk & 3) * 32, 16, 1024), idesc_qk, 1u);
-      }
-      ptx::mma_commit(&bar[pass]);
-    }
-  }
-  if (ok) ok = ptx::mbar_wait_bounded(&bar[1], 0, &abort_flag);
+  for (int b = 0; b < 4; ++b) ok = ok && ptx::mbar_wait_bounded(&bar[b], 0, &abort_flag);
   ptx::tc_fence_after();
-  // P over the rope chunk: row = token, 64 heads x fp16 = 128 B (MN-major for the PV B operand)
-  for (int u = 0; u < 8; ++u) ptx::sts128(k_base + 8 * kKChunk + swz(t, u), reinterpret_cast<const uint4*>(P)[t * 8 + u]);
+  if (ok) {
+    float v[NH];
+    for (int b = 0; b < 4; ++b) {
+      read_cols<NH>(tmem, C::kSCol + NH * b, NH, v);
+      for (int h = 0; h < NH; ++h) S_out[((size_t)b * 128 + t) * NH + h] = v[h];
+    }
+  }
+
+  // PV of block 0 with its operand in the rope chunk (free once the QK completed)
+  write_pm<NH>(bufR, Pm);
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (t == 0 && ok) {
-    for (int j = 0; j < 4; ++j)
-      for (int kk = 0; kk < 8; ++kk)
-        ptx::mma_f16_ss(tmem + 64 * j, ptx::sw128_desc(k_base + 2 * j * kKChunk + kk * 2048, kKChunk, 1024),
-                        ptx::sw128_desc(k_base + 8 * kKChunk + kk * 2048, 1024, 1024), ptx::idesc_f16(128, kHeads, 1, 1),
-                        kk != 0);
-    ptx::mma_commit(&bar[2]);
-  }
-  if (ok) ok = ptx::mbar_wait_bounded(&bar[2], 0, &abort_flag);
-  ptx::tc_fence_after();
-  uint32_t r[32];
-  for (int hh = 0; hh < 2; ++hh) {
-    ptx::tmem_ld32(tmem + lane_base + 256 + 32 * hh, r);
-    ptx::tmem_wait_ld();
-    for (int q = 0; q < 32; ++q) S_out[t * kHeads + 32 * hh + q] = __uint_as_float(r[q]);
-  }
-  for (int j = 0; j < 4; ++j)
-    for (int hh = 0; hh < 2; ++hh) {
-      ptx::tmem_ld32(tmem + lane_base + 64 * j + 32 * hh, r);
-      ptx::tmem_wait_ld();
-      for (int q = 0; q < 32; ++q) O_out[(128 * j + t) * kHeads + 32 * hh + q] = __uint_as_float(r[q]);
+  if (warp == 0 && ok) {
+    if (ptx::elect_one()) {
+      issue_pv<NH, 0>(tmem, dV, desc_pm<NH>(bufR), false);
+      ptx::mma_commit(&bar[4]);
     }
+    __syncwarp();
+  }
+  ok = ok && ptx::mbar_wait_bounded(&bar[4], 0, &abort_flag);
+  // blocks 1..3 with their operands in chunks 0, rope and 1 (block 0's V is no longer read)
+  write_pm<NH>(buf0, Pm + 1 * 128 * NH);
+  write_pm<NH>(bufR, Pm + 2 * 128 * NH);
+  write_pm<NH>(buf1, Pm + 3 * 128 * NH);
+  ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (warp == 0 && ok) {
+    if (ptx::elect_one()) {
+      issue_pv<NH, 1>(tmem, dV, desc_pm<NH>(buf0), false);
+      issue_pv<NH, 2>(tmem, dV, desc_pm<NH>(bufR), false);
+      issue_pv<NH, 3>(tmem, dV, desc_pm<NH>(buf1), false);
+      ptx::mma_commit(&bar[5]);
+    }
+    __syncwarp();
+  }
+  ok = ok && ptx::mbar_wait_bounded(&bar[5], 0, &abort_flag);
+  ptx::tc_fence_after();
+  if (ok) {
+    // O^T in chunks of kChunkCols columns, as the kernel's epilogue reads it: chunk c holds block
+    // (kChunkCols c) / NH, heads (kChunkCols c) % NH ..; TMEM lane = dim within the block
+    float v[C::kChunkCols];
+    for (int c = 0; c < C::kChunks; ++c) {
+      const int jb = (C::kChunkCols * c) / NH, hb = (C::kChunkCols * c) % NH;
+      read_cols<NH>(tmem, C::kChunkCols * c, C::kChunkCols, v);
+      for (int h = 0; h < C::kChunkCols; ++h) O_out[(size_t)(128 * jb + t) * NH + hb + h] = v[h];
+    }
+  }
   if (t == 0) *status = ok ? 0 : 1;
-  if (warp == 0) ptx::tmem_dealloc(tmem, 512);
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 0) ptx::tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int NH>
+int run(const uint16_t* K, const uint16_t* Q, const uint16_t* Pm, float* S, float* O, int* status) {
+  const size_t smem = selftest_smem<NH>();
+  if (cudaFuncSetAttribute(selftest_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return 1;
+  selftest_kernel<NH><<<1, 128, smem>>>(K, Q, Pm, S, O, status);
+  if (cudaGetLastError() != cudaSuccess) return 2;
+  return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
 }
 
 }  // namespace
 
-extern "C" int tc_selftest(const void* A, const void* Q, const void* L, const void* P, float* S, float* O,
-                           int* status) {
-  const int smem = 226 * 1024;   // plus the static barriers, within the 227 KB opt-in limit
-  if (cudaFuncSetAttribute(selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return 1;
-  selftest_kernel<<<1, 128, smem>>>(static_cast<const uint16_t*>(A), static_cast<const uint16_t*>(Q),
-                                    static_cast<const uint16_t*>(L), static_cast<const uint16_t*>(P), S, O, status);
-  if (cudaGetLastError() != cudaSuccess) return 2;
-  return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
+// K fp16 [128][576], Q fp16 [nh][576], Pm fp16 [4][128][nh]; S fp32 [4][128][nh], O fp32 [512][nh].
+extern "C" int tc_selftest(int nh, const void* K, const void* Q, const void* Pm, float* S, float* O, int* status) {
+  const uint16_t* k = static_cast<const uint16_t*>(K);
+  const uint16_t* q = static_cast<const uint16_t*>(Q);
+  const uint16_t* pm = static_cast<const uint16_t*>(Pm);
+  switch (nh) {
+    case 16: return run<16>(k, q, pm, S, O, status);
+    case 32: return run<32>(k, q, pm, S, O, status);
+    case 64: return run<64>(k, q, pm, S, O, status);
+    default: return 4;
+  }
 }

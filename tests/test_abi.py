@@ -70,6 +70,33 @@ def test_host_side_rejections(lib):
     assert lib.sparse_mla_workspace_size(None, 2) == 0
 
 
+def test_noalloc_dims_statuses_match_the_workspace_entry_point(lib):
+    """The workspace-free decode checks dims the way sparse_mla_decode does, before any CUDA call."""
+    for dims, want in ((make_dims(4, 48, 512, 16, 100, nsplit=4), 2),      # unsupported head count
+                       (make_dims(4, 48, 512, 16, 100, nsplit=0), 2),
+                       (make_dims(4, 64, 4096, 16, 100, nsplit=2), 2),     # top-k too long
+                       (make_dims(0, 64, 512, 16, 100, nsplit=0), 1)):     # no queries
+        assert _decode(lib, dims) == want
+        assert lib.sparse_mla_decode_noalloc(C.byref(dims), FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04),
+                                             FAKE, FAKE, None) == want
+    assert lib.sparse_mla_decode_noalloc(None, FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,
+                                         None) == 1
+    assert lib.sparse_mla_noalloc_read_errors(None, None) == 1
+
+
+def test_debug_entry_points_host_checks(lib):
+    d = make_dims(4, 64, 512, 16, 100, nsplit=4)
+    assert lib.sparse_mla_decode_rows(C.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,
+                                      FAKE, C.c_size_t(1 << 30), None, None) == 1            # no row buffer
+    assert lib.sparse_mla_decode_rows(C.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,
+                                      FAKE, C.c_size_t(1 << 30), C.c_void_p((1 << 20) + 4), None) == 1
+    bad = make_dims(4, 48, 512, 16, 100, nsplit=4)
+    assert lib.sparse_mla_decode_rows(C.byref(bad), FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,
+                                      FAKE, C.c_size_t(1 << 30), FAKE, None) == 2
+    assert lib.sparse_mla_debug_set_wait_limit(5) == 0
+    assert lib.sparse_mla_debug_set_wait_limit(0) == 0     # back to the default
+
+
 def _plan(lib, B, H, K, sms, nsplit=0):
     p = _native.SmlaPlan()
     st = lib.sparse_mla_plan_for(C.byref(make_dims(B, H, K, 8192, 1 << 20, nsplit)), sms, C.byref(p))

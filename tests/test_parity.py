@@ -165,14 +165,41 @@ def _sample(B, n, seed):
     return sorted(rng.choice(B, size=min(n, B), replace=False).tolist())
 
 
-@pytest.mark.parametrize("name", ["bs1_ctx8k", "b32_ctx32k", "b80_ctx128k", "b96_ragged_h64", "b96_ragged_h16"])
+def _decode_rows(w, nsplit=0, heads_per_cta=0):
+    """Decode that also returns the rows its split kernel loaded; the row buffer starts as a sentinel
+    no entry can produce, so an entry the kernel never resolved shows up."""
+    rows = torch.full(tuple(w.topk_idx.shape), -7, dtype=torch.int64, device=DEV)
+    out, lse, rows = api.sparse_mla_decode_rows(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens,
+                                                w.sm_scale, nsplit=nsplit, heads_per_cta=heads_per_cta, rows=rows)
+    torch.cuda.synchronize()
+    return out, lse, rows
+
+
+@pytest.mark.parametrize("nh", [16, 32, 64])
+@pytest.mark.parametrize("nsplit", [1, 3, 4])
+def test_decode_gathers_exactly_the_oracle_rows(nh, nsplit):
+    # the rows the decode kernel itself loaded, bit-exact: several tiles per partition, ragged tails,
+    # padding, entries at or past the length, duplicates, pages outside the table and the cache
+    w = _custom(B=5, H=64, topk=448, ctx=[5000, 300, 64, 1, 2000], seed=90 + nh + nsplit)
+    w.topk_idx[0, :6] = torch.tensor([7, 7, 4999, 5000, -1, 130], dtype=torch.int32, device=DEV)
+    w.block_table[4, 3] = w.num_pages + 2               # a physical page outside the cache
+    out, lse, rows = _decode_rows(w, nsplit=nsplit, heads_per_cta=nh)
+    assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))
+    compare(out, lse, *oracle_on(w))
+
+
+@pytest.mark.parametrize("name", ["tiny", "bs1_ctx8k", "b32_ctx32k", "b80_ctx128k", "b96_ragged_h64",
+                                  "b96_ragged_h16"])
 def test_full_size_configs_sampled(name):
     """The full configurations with the scheduler's launch choice (the one the benchmark times):
-    every gathered row index is bit-exact for all queries; out and lse are checked against the oracle on
-    sampled queries (the oracle copies only the pages those queries touch)."""
+    every row the decode kernel gathered is bit-exact for all queries; out and lse are checked against
+    the oracle on sampled queries (the oracle copies only the pages those queries touch)."""
     w = wl.make_workload(wl.CONFIGS[name], device=DEV)
     try:
         out, lse = _run(w)
+        out_r, lse_r, rows = _decode_rows(w)
+        assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))
+        assert torch.equal(out_r, out) and torch.equal(lse_r, lse)    # recording rows changes nothing else
         rows = api.sparse_mla_gather_rows(w.block_table, w.topk_idx, w.seq_lens, w.num_pages)
         torch.cuda.synchronize()
         assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))

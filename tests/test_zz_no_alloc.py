@@ -11,7 +11,7 @@ import torch
 
 from sparse_mla_decode_paged_gb300 import _native, api
 from sparse_mla_decode_paged_gb300 import workloads as wl
-from parity_util import LSE_ATOL, OUT_RTOL
+from parity_util import LSE_ATOL, OUT_RTOL, compare, oracle_on
 
 pytestmark = pytest.mark.gpu
 
@@ -56,3 +56,29 @@ def test_noalloc_rejects_shapes_beyond_the_scratch():
     assert _noalloc(lib, w, 16, out, lse) == 3          # SMLA_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
     assert torch.all(out == 0)
+
+
+def _flags(lib):
+    v = C.c_uint32(0xFFFFFFFF)
+    assert lib.sparse_mla_noalloc_read_errors(C.byref(v), api._stream()) == 0
+    return int(v.value)
+
+
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_noalloc_matches_the_oracle_and_reports_bad_pages(nsplit):
+    """Checked against the float64 oracle directly; a block-table entry outside the cache sets the
+    page-range flag, which the error getter reads back, and the next clean call clears it."""
+    lib = _native.load()
+    w = wl.make_custom(B=3, H=64, topk=300, ctx_lens=[2000, 700, 90], seed=81 + nsplit, device="cuda")
+    w.block_table[1, 2] = w.num_pages + 11
+    out = torch.empty((w.B, w.H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.H), dtype=torch.float32, device="cuda")
+    assert _noalloc(lib, w, nsplit, out, lse) == 0
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle_on(w))
+    assert _flags(lib) & _native.DEVERR_PAGE_RANGE
+    clean = wl.make_custom(B=3, H=64, topk=300, ctx_lens=[2000, 700, 90], seed=81 + nsplit, device="cuda")
+    assert _noalloc(lib, clean, nsplit, out, lse) == 0
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle_on(clean))
+    assert _flags(lib) == 0
