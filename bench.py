@@ -197,7 +197,8 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- our arm
 
 class Bench:
-    def __init__(self, name: str, device, seed_offset: int = 0, nsplit: int = 0):
+    def __init__(self, name: str, device, seed_offset: int = 0, nsplit: int = 0, merge: int = 0,
+                 heads_per_cta: int = 0):
         import torch
         from sparse_mla_decode_paged_gb300 import api
         from sparse_mla_decode_paged_gb300 import workloads as wl
@@ -216,8 +217,7 @@ class Bench:
         self.R = int(min(2048, max(8, math.ceil(4 * l2 / self.bytes_per_call))))
         self.sets = [w0] + [wl.make_workload(spec, device=device, rotation=r, kv_cache=self.cache)
                             for r in range(1, self.R)]
-        self.dims = api.dims_of(w0.q, w0.kv_cache, w0.block_table, w0.topk_idx, 0)
-        self.dims.nsplit = nsplit
+        self.dims = api.dims_of(w0.q, w0.kv_cache, w0.block_table, w0.topk_idx, nsplit, heads_per_cta, merge)
         self.plan = api.plan(self.dims, device.index if hasattr(device, "index") else None)
         self.nsplit = self.plan.nsplit
         self.dims.nsplit = self.nsplit
@@ -231,9 +231,14 @@ class Bench:
     def call(self, i: int):
         w = self.sets[i % self.R]
         self.api.sparse_mla_decode(w.q, self.cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
-                                   out=self.out, lse=self.lse, workspace=self.ws, nsplit=self.nsplit)
+                                   out=self.out, lse=self.lse, workspace=self.ws, nsplit=self.nsplit,
+                                   heads_per_cta=self.plan.heads_per_cta, merge=self.dims.merge)
 
     def split_only(self, i: int):
+        """The split kernel as the call launches it: the call itself when that is one launch (one partition,
+        or the partitions merged inside the kernel), else the split kernel writing its partials."""
+        if self.nsplit == 1 or self.plan.fused:
+            return self.call(i)
         w = self.sets[i % self.R]
         d = self.dims
         lib = self.api._lib()
@@ -285,7 +290,7 @@ class Bench:
         self.api.sparse_mla_topk_select(s, self.tk_lens, self.tk_out.shape[1])
 
     def launches_per_call(self) -> int:
-        return 1 + (1 if self.nsplit > 1 else 0)
+        return 1 + (1 if self.nsplit > 1 and not self.plan.fused else 0)
 
     def _graph(self, fn, start: int, n: int):
         torch = self.torch
@@ -383,7 +388,8 @@ class Bench:
                 if not first:
                     s_comp.wait_event(read[k])
                 self.api.sparse_mla_decode(dq, self.cache, dbt, dtk, dsl, w0.sm_scale, out=out, lse=lse,
-                                           workspace=wss[k], nsplit=self.nsplit, stream=s_comp)
+                                           workspace=wss[k], nsplit=self.nsplit, stream=s_comp,
+                                           heads_per_cta=self.plan.heads_per_cta, merge=self.dims.merge)
                 computed[k].record(s_comp)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(computed[k])

@@ -93,6 +93,11 @@ typedef struct smla_dims {
   int32_t queries_per_request;/* s_q >= 1 (0 means 1): query b reads block_table row     */
                               /* b / s_q (several queries of one request, each with its  */
                               /* own top-k and seq_lens entry); batch must be a multiple */
+  int32_t merge;              /* how partitions are merged when nsplit > 1: 0 = the      */
+                              /* scheduler's choice, 1 = the merge kernel, 2 = inside    */
+                              /* the split kernel (a cluster of the nsplit CTAs; needs   */
+                              /* nsplit <= 8 dividing heads_per_cta <= H, else           */
+                              /* SMLA_ERR_UNSUPPORTED)                                   */
 } smla_dims;
 
 typedef struct smla_plan {
@@ -107,6 +112,9 @@ typedef struct smla_plan {
   double est_us;              /* cost-model estimate of one call, microseconds           */
   size_t workspace_bytes;     /* bytes sparse_mla_decode needs with this plan            */
   int32_t heads_per_cta;      /* heads per CTA of the split kernel: 16, 32 or 64 (<= H)  */
+  int32_t fused;              /* 1: the nsplit partitions of a (query, head group) run as */
+                              /* one thread-block cluster and merge inside the split     */
+                              /* kernel (no merge launch); 0: merge kernel when nsplit>1 */
 } smla_plan;
 
 /* Split-count scheduler, host only, no CUDA calls.  Chooses nsplit (unless

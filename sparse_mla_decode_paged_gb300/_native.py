@@ -13,7 +13,7 @@ class SmlaDims(C.Structure):
     _fields_ = [("batch", C.c_int32), ("num_heads", C.c_int32), ("topk", C.c_int32),
                 ("page_size", C.c_int32), ("max_pages_per_seq", C.c_int32), ("d_latent", C.c_int32),
                 ("d_rope", C.c_int32), ("nsplit", C.c_int32), ("num_pages", C.c_int64),
-                ("heads_per_cta", C.c_int32), ("queries_per_request", C.c_int32)]
+                ("heads_per_cta", C.c_int32), ("queries_per_request", C.c_int32), ("merge", C.c_int32)]
 
 
 class SmlaAppendDims(C.Structure):
@@ -31,7 +31,7 @@ class SmlaPlan(C.Structure):
     _fields_ = [("nsplit", C.c_int32), ("tokens_per_split", C.c_int32), ("head_groups", C.c_int32),
                 ("ctas", C.c_int32), ("ctas_per_sm", C.c_int32), ("sm_count", C.c_int32),
                 ("waves", C.c_double), ("est_us", C.c_double), ("workspace_bytes", C.c_size_t),
-                ("heads_per_cta", C.c_int32)]
+                ("heads_per_cta", C.c_int32), ("fused", C.c_int32)]
 
 
 _P = C.c_void_p

@@ -40,16 +40,20 @@ def _need(t: torch.Tensor, name: str, dtype, ndim: int):
         raise ValueError(f"{name} must be a contiguous {ndim}-d tensor")
 
 
+MERGE_AUTO, MERGE_KERNEL, MERGE_FUSED = 0, 1, 2
+
+
 def make_dims(B: int, H: int, topk: int, max_pages_per_seq: int, num_pages: int, nsplit: int = 0,
-              heads_per_cta: int = 0, queries_per_request: int = 1) -> SmlaDims:
+              heads_per_cta: int = 0, queries_per_request: int = 1, merge: int = MERGE_AUTO) -> SmlaDims:
     return SmlaDims(B, H, topk, PAGE_SIZE, max_pages_per_seq, D_LATENT, D_ROPE, nsplit, num_pages, heads_per_cta,
-                    queries_per_request)
+                    queries_per_request, merge)
 
 
-def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0, heads_per_cta: int = 0) -> SmlaDims:
+def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0, heads_per_cta: int = 0,
+            merge: int = MERGE_AUTO) -> SmlaDims:
     """Shapes of a call; several queries per request when q has a multiple of block_table's rows."""
     return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit,
-                     heads_per_cta, q.shape[0] // block_table.shape[0])
+                     heads_per_cta, q.shape[0] // block_table.shape[0], merge)
 
 
 def plan_for(dims: SmlaDims, sm_count: int) -> SmlaPlan:
@@ -93,12 +97,13 @@ def _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens):
 def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor, topk_idx: torch.Tensor,
                       seq_lens: torch.Tensor, sm_scale: float, out: Optional[torch.Tensor] = None,
                       lse: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                      nsplit: int = 0, stream=None, heads_per_cta: int = 0) -> Tuple[torch.Tensor, torch.Tensor]:
-    """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0 and heads_per_cta = 0 let the library's
-    scheduler choose."""
+                      nsplit: int = 0, stream=None, heads_per_cta: int = 0,
+                      merge: int = MERGE_AUTO) -> Tuple[torch.Tensor, torch.Tensor]:
+    """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0, heads_per_cta = 0 and merge = MERGE_AUTO let the
+    library's scheduler choose."""
     _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
     B, H = q.shape[0], q.shape[1]
-    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta)
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta, merge)
     if nsplit == 0:
         nsplit = plan(dims, q.device.index).nsplit
         dims.nsplit = nsplit
@@ -118,12 +123,12 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
 def sparse_mla_decode_rows(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                            topk_idx: torch.Tensor, seq_lens: torch.Tensor, sm_scale: float,
                            workspace: Optional[torch.Tensor] = None, nsplit: int = 0, stream=None,
-                           heads_per_cta: int = 0, rows: Optional[torch.Tensor] = None):
+                           heads_per_cta: int = 0, rows: Optional[torch.Tensor] = None, merge: int = MERGE_AUTO):
     """sparse_mla_decode that also returns the rows the decode's split kernel loaded:
     (out bf16 [B,H,512], lse fp32 [B,H], rows int64 [B,topk], -1 for skipped entries)."""
     _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
     B, H = q.shape[0], q.shape[1]
-    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta)
+    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta, merge)
     if nsplit == 0:
         nsplit = plan(dims, q.device.index).nsplit
         dims.nsplit = nsplit

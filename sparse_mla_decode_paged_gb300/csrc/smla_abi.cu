@@ -29,6 +29,7 @@ int check_decode_dims(const smla_dims* d) {
   if (d->heads_per_cta != 0 && !split_heads_supported(d->heads_per_cta)) return SMLA_ERR_INVALID_ARG;
   if (d->queries_per_request < 0 || (d->queries_per_request > 1 && d->batch % d->queries_per_request != 0))
     return SMLA_ERR_INVALID_ARG;
+  if (d->merge < 0 || d->merge > 2) return SMLA_ERR_INVALID_ARG;
   if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
   if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
   if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
@@ -117,13 +118,14 @@ int decode_impl(const smla_dims* dims, const void* q, const void* kv_cache, cons
   p.lse = lse;
   p.rows_out = rows_out;
   p.final_out = (nsplit == 1);
+  p.fused = plan.fused != 0;
   if (nsplit > 1) {
     const size_t lse_bytes = ((size_t)dims->batch * nsplit * dims->num_heads * sizeof(float) + 255) / 256 * 256;
     p.lse_part = reinterpret_cast<float*>(ws + kWorkspaceHeader);
     p.o_part = reinterpret_cast<float*>(ws + kWorkspaceHeader + lse_bytes);
   }
   if (launch_split(p, s) != cudaSuccess) return SMLA_ERR_CUDA;
-  if (nsplit > 1 &&
+  if (nsplit > 1 && !p.fused &&
       launch_combine(dims->batch, dims->num_heads, nsplit, p.o_part, p.lse_part, p.out, lse, s) != cudaSuccess)
     return SMLA_ERR_CUDA;
   return SMLA_OK;

@@ -17,6 +17,7 @@ constexpr int kMaxTopk = 2048;
 constexpr int kMaxSplit = 16;
 constexpr int kMaxCombineSplit = 64;
 constexpr size_t kWorkspaceHeader = 256;
+constexpr int kMaxFusedSplit = 8;      // partitions merged inside the split kernel (one portable cluster)
 
 // Everything the split kernels need for one launch.
 struct SplitParams {
@@ -38,6 +39,8 @@ struct SplitParams {
   float* o_part;              // [B][nsplit][H][512]
   float* lse_part;            // [B][nsplit][H]
   uint32_t* err;              // device error word (may be null)
+  bool fused;                 // nsplit > 1 merged inside the kernel: the nsplit CTAs of a (query, head
+                              // group) form one cluster; o_part is their exchange area, out/lse the result
   int64_t* rows_out;          // [B][topk] or null: the row the gather warps resolved for each entry
   uint64_t wait_ns;           // time limit of each pipeline wait inside the kernel
 };
@@ -98,5 +101,8 @@ int split_ctas_per_sm(int H);
 bool split_heads_supported(int nh);
 // CTAs per work unit (one unit per query, partition and head group).
 int split_ctas_per_unit();
+// Whether the split kernel merges nsplit partitions itself for nh heads per CTA and H heads (a cluster of
+// nsplit CTAs, each owning nh / nsplit heads of the merge).
+bool split_fusable(int nsplit, int nh, int H);
 
 }  // namespace smla

@@ -115,6 +115,16 @@ __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   return r;
 }
 
+// 32-bit store into the shared memory of another CTA of the cluster (address from mapa).
+__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+
+// Split cluster barrier: every thread arrives once (relaxed: no ordering of earlier accesses) and later
+// waits; used to know that every CTA of the cluster has started before its shared memory is written.
+__device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 // Every thread of every CTA of the cluster (non-aligned forms).
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
@@ -134,6 +144,10 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, v
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+
+// Orders this thread's accesses through the async proxy (bulk copies) and the generic proxy in every
+// state space: after a completed bulk store, before a release; after an acquire, before a bulk load.
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
 
 // Named barrier over `threads` threads (non-aligned form: lanes of a warp may arrive separately).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
@@ -287,6 +301,18 @@ __device__ __forceinline__ int ldg_i32_now(const int32_t* p) {
   return v;
 }
 
+// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory to global memory, tracked by the
+// issuing thread's bulk groups.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until every committed bulk group of this thread has completed (its global writes performed).
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Programmatic dependent launch: a grid launched with programmatic stream serialization after this
 // one may start once every CTA here has signalled (or exited); it waits for this grid's completion
 // and memory with griddep_wait before touching its results.
@@ -311,6 +337,21 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ void sts32f(uint32_t saddr, float v) {
+  asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void sts16(uint32_t saddr, uint16_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(v) : "memory");
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t saddr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
+               : "memory");
+  return v;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t saddr) {

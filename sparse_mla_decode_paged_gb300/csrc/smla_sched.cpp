@@ -29,7 +29,19 @@ struct CostModel {
   double partial_extra_us_per_head = 0.7 / 64;         // fp32 partial rows instead of bf16 output
   double combine_fixed_us = 2.0;       // merge kernel: launch (overlapped with the split kernel's tail)
   double combine_gbs = 6000.0;
+  // merge inside a cluster: a fixed part (two cluster barriers, the lse exchange) plus the weighted fp32
+  // rows each CTA bulk-stores for its peers and bulk-loads from them, at a per-SM rate
+  double fused_fixed_us = 1.0;
+  double fused_bytes_per_us = 64e3;
 };
+
+// Clusters of `csize` CTAs (one CTA per SM) that fit at once: the SMs of a GPC that a cluster size does not
+// divide stay idle, so larger clusters fill fewer SMs (152 SMs: 76, 36 and 15 clusters of 2, 4 and 8).
+static int clusters_per_wave(int csize, int sm_count) {
+  const double fill = csize <= 2 ? 1.0 : csize <= 4 ? 0.95 : 0.8;
+  const int n = (int)(fill * sm_count / csize + 1e-9);
+  return n > 0 ? n : 1;
+}
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -39,6 +51,7 @@ static bool dims_valid(const smla_dims* d) {
   if (d->nsplit < 0) return false;
   if (d->heads_per_cta != 0 && d->heads_per_cta != 16 && d->heads_per_cta != 32 && d->heads_per_cta != 64)
     return false;
+  if (d->merge < 0 || d->merge > 2) return false;
   return true;
 }
 
@@ -61,21 +74,30 @@ size_t workspace_bytes_for(int B, int H, int nsplit) {
 
 static int nh_index(int nh) { return nh == 16 ? 0 : nh == 32 ? 1 : 2; }
 
-static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len, int nh,
+static double estimate_us(const CostModel& m, int B, int H, int topk, int nsplit, int split_len, int nh, bool fused,
                           int sm_count, int ctas_per_sm, int* ctas_out, double* waves_out) {
   const int head_groups = (H + nh - 1) / nh;
   const int ctas = B * head_groups * nsplit * split_ctas_per_unit();
   const double slots = (double)sm_count * ctas_per_sm;
   const double waves = ctas / slots;
-  const int whole_waves = (int)ceil(waves - 1e-9);
+  int whole_waves = (int)ceil(waves - 1e-9);
+  if (fused) {
+    const int clusters = B * head_groups, per_wave = clusters_per_wave(nsplit, sm_count);
+    whole_waves = (clusters + per_wave - 1) / per_wave;
+  }
   const int tokens = split_len < topk ? split_len : topk;
   const int k = nh_index(nh);
   double cta_us = m.cta_fixed_us + m.epilogue_us_per_head * nh;
   for (int left = tokens; left > 0; left -= 128)
     cta_us += m.tile_fixed_us[k] + m.tile_token_us[k] * (left < 128 ? left : 128);
-  if (nsplit > 1) cta_us += m.partial_extra_us_per_head * nh;
+  if (fused) {
+    const double moved = 2.0 * nh * (nsplit - 1) / nsplit * kDLatent * 4.0;
+    cta_us += m.fused_fixed_us + moved / m.fused_bytes_per_us;
+  } else if (nsplit > 1) {
+    cta_us += m.partial_extra_us_per_head * nh;
+  }
   double t = whole_waves * cta_us;
-  if (nsplit > 1) {
+  if (nsplit > 1 && !fused) {
     const double bytes = (double)B * H * (nsplit * (kDLatent * 4.0 + 4.0) + kDLatent * 2.0 + 4.0);
     t += m.combine_fixed_us + bytes / (m.combine_gbs * 1e3);
   }
@@ -96,6 +118,7 @@ extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla
   const int B = dims->batch, H = dims->num_heads, K = dims->topk;
   const int cps = split_ctas_per_sm(H);
   int best_n = -1, best_len = 0, best_ctas = 0, best_nh = 0;
+  bool best_fused = false;
   double best_t = 0, best_w = 0;
   int lo = 1, hi = kMaxSplit;
   if (dims->nsplit > 0) lo = hi = dims->nsplit;
@@ -109,14 +132,21 @@ extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla
       const int len = split_len_for(K, n);
       // an automatic choice never leaves a partition empty; a fixed one is kept as given
       if (dims->nsplit == 0 && (K + len - 1) / len != n) continue;
-      int ctas;
-      double w;
-      const double t = estimate_us(m, B, H, K, n, len, nh, sm_count, cps, &ctas, &w);
-      if (best_n < 0 || t < best_t - 1e-9) {
-        best_n = n; best_len = len; best_t = t; best_ctas = ctas; best_w = w; best_nh = nh;
+      // the merge kernel, or the merge inside a cluster of the partitions where the kernel supports it
+      for (int f = 0; f < 2; ++f) {
+        if (f == 1 && !split_fusable(n, nh, H)) continue;
+        if (dims->merge == 1 && f == 1) continue;                 // the merge kernel asked for
+        if (dims->merge == 2 && f == 0 && n > 1) continue;        // the in-kernel merge asked for
+        int ctas;
+        double w;
+        const double t = estimate_us(m, B, H, K, n, len, nh, f == 1, sm_count, cps, &ctas, &w);
+        if (best_n < 0 || t < best_t - 1e-9) {
+          best_n = n; best_len = len; best_t = t; best_ctas = ctas; best_w = w; best_nh = nh; best_fused = f == 1;
+        }
       }
     }
   }
+  if (best_n < 0) return SMLA_ERR_UNSUPPORTED;                   // an in-kernel merge no shape allows
   memset(plan, 0, sizeof(*plan));
   plan->nsplit = best_n;
   plan->tokens_per_split = best_len;
@@ -128,6 +158,7 @@ extern "C" int sparse_mla_plan_for(const smla_dims* dims, int32_t sm_count, smla
   plan->waves = best_w;
   plan->est_us = best_t;
   plan->workspace_bytes = workspace_bytes_for(B, H, best_n);
+  plan->fused = best_fused ? 1 : 0;
   return SMLA_OK;
 }
 

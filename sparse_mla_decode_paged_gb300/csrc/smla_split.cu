@@ -90,6 +90,11 @@ struct Misc {
   alignas(16) float red[kSoftWarps][kHeadsMax];
   alignas(16) float linv[kHeadsMax];
   float lse_out[kHeadsMax];
+  // merge inside a cluster of the query's partitions
+  uint64_t merge_in;                     // peers' weighted rows of this CTA's head slice landed
+  alignas(16) float lse_all[kMaxFusedSplit][kHeadsMax];   // every partition's lse (pushed by each CTA)
+  alignas(16) float wts[kMaxFusedSplit][kHeadsMax / 2];   // merge weights of this CTA's heads (at most NH / 2)
+  alignas(16) float lse_merged[kHeadsMax / 2];
 };
 
 template <int NH>
@@ -642,21 +647,70 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 }
 
 // ------------------------------------------------------------------------------------------ epilogue
-// All 12 warps write O / l from TMEM straight to the output rows [head][512] (bf16, or fp32
-// partials): warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and the
-// column chunks c = w / 4, w / 4 + 3, ... of O^T (chunks of 32 columns, 16 for NH = 16; block
-// c * cols / NH).  Lanes 2j, 2j + 1 hold dims d, d + 1; for heads h, h + 1 the even lane writes row h
-// and the odd lane row h + 1, two dims each.
-template <int NH>
-__device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane) {
+// O^T from TMEM, scaled per head by scale[h] (1/l, or the merge weight of this partition), staged as rows
+// [head][512] at `stage` (the K tile, free once every PV MMA has completed): fp32 rows of 2048 bytes or
+// bf16 rows of 1024 bytes.  Warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim
+// block) and the column chunks w / 4, w / 4 + 3, ... of O^T (chunks of 32 columns, 16 for NH = 16; block
+// c * cols / NH); lane l writes dim d of every head of the chunk, so a warp's store covers 32
+// consecutive dims of one row.
+template <int NH, bool kF32>
+__device__ __forceinline__ void stage_rows(const Ctx& x, int warp, int lane, uint32_t stage, const float* scale) {
   using C = Cfg<NH>;
   constexpr int kCols = C::kChunkCols;
-  const SplitParams& p = *x.p;
-  Misc& ms = *x.ms;
+  const int quad = warp & 3;
+  const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
+#pragma unroll 1
+  for (int c = warp >> 2; c < C::kChunks; c += 3) {
+    const int jb = (kCols * c) / NH, hb = (kCols * c) % NH;
+    uint32_t r[kCols];
+    if constexpr (kCols == 16) ptx::tmem_ld16(x.tmem + lane_q + kCols * c, r);
+    else ptx::tmem_ld32(x.tmem + lane_q + kCols * c, r);
+    float v[kCols];
+#pragma unroll
+    for (int k = 0; k < kCols / 4; ++k) {
+      const float4 l4 = reinterpret_cast<const float4*>(scale + hb)[k];
+      v[4 * k] = l4.x; v[4 * k + 1] = l4.y; v[4 * k + 2] = l4.z; v[4 * k + 3] = l4.w;
+    }
+    ptx::tmem_wait_ld();
+    const uint32_t d = 128 * jb + 32 * quad + lane;
+#pragma unroll
+    for (int h = 0; h < kCols; ++h) {
+      const float o = v[h] * __uint_as_float(r[h]);
+      if constexpr (kF32) ptx::sts32f(stage + (uint32_t)(hb + h) * 2048u + 4u * d, o);
+      else ptx::sts16(stage + (uint32_t)(hb + h) * 1024u + 2u * d, (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu));
+    }
+  }
+}
+
+// Rows [0, rows) of `row_bytes` each, staged contiguously at `stage`, to contiguous global rows at dst: the
+// lanes of warp 0 each bulk-copy four rows, then wait until the copies have read shared memory (the
+// global writes complete before the grid does).  Call after a proxy fence and a CTA barrier.
+__device__ __forceinline__ void store_rows(void* dst, uint32_t stage, int rows, uint32_t row_bytes, int warp, int lane) {
+  if (warp != 0) return;
+  const int r0 = 4 * lane;
+  if (r0 < rows) {
+    const int n = min(4, rows - r0);
+    ptx::bulk_s2g(static_cast<unsigned char*>(dst) + (size_t)r0 * row_bytes, stage + (uint32_t)r0 * row_bytes,
+                  (uint32_t)n * row_bytes);
+    ptx::bulk_commit();
+    ptx::bulk_wait_read_all();
+  }
+}
+
+// O / l in fp32 from TMEM: rows of heads outside [keep_lo, keep_lo + keep_n) go straight to global
+// memory at dst (row h at dst + h * 512), rows inside it are staged in shared memory at `stage` (row h -
+// keep_lo, 2048 bytes each).  Warp w reads TMEM lane quadrant w % 4 and the column chunks w / 4, w / 4 + 3,
+// ... of O^T (as stage_rows); lanes 2j, 2j + 1 hold dims d, d + 1 and exchange one value per head pair, so
+// each global store writes two dims of one row (a warp's store covers two rows of 64 bytes).
+template <int NH>
+__device__ __forceinline__ void write_rows_f32(const Ctx& x, int warp, int lane, float* dst, int rows,
+                                               uint32_t stage, int keep_lo, int keep_n) {
+  using C = Cfg<NH>;
+  constexpr int kCols = C::kChunkCols;
+  const Misc& ms = *x.ms;
   const int quad = warp & 3;
   const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
   const bool odd = lane & 1;
-  const size_t head0 = (size_t)x.g * NH;
 #pragma unroll 1
   for (int c = warp >> 2; c < C::kChunks; c += 3) {
     const int jb = (kCols * c) / NH, hb = (kCols * c) % NH;
@@ -672,24 +726,112 @@ __device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane)
     ptx::tmem_wait_ld();
 #pragma unroll
     for (int h = 0; h < kCols; ++h) v[h] *= __uint_as_float(r[h]);
-    const int d0 = 128 * jb + 32 * quad + (lane & ~1);
+    const uint32_t d = 128 * jb + 32 * quad + lane;
+    const int d0 = (int)(d & ~1u);
 #pragma unroll
     for (int h = 0; h < kCols; h += 2) {
-      const float mine = odd ? v[h + 1] : v[h];
-      const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
-      const float lo = odd ? other : mine, hi = odd ? mine : other;   // dims d0, d0 + 1
-      const int hl = hb + h + (odd ? 1 : 0);
-      if (hl < x.hg_valid) {
-        if (p.final_out) {
-          uint16_t* dst = p.out + ((size_t)x.b * p.H + head0 + hl) * kDLatent + d0;
-          *reinterpret_cast<uint32_t*>(dst) = f32x2_to_bf16x2(lo, hi);
-        } else {
-          float* dst = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + head0 + hl) * kDLatent + d0;
-          *reinterpret_cast<float2*>(dst) = make_float2(lo, hi);
-        }
+      const int h0 = hb + h;                  // a head pair lies inside or outside the kept range together
+      if (h0 >= keep_lo && h0 < keep_lo + keep_n) {
+        ptx::sts32f(stage + (uint32_t)(h0 - keep_lo) * 2048u + 4u * d, v[h]);
+        ptx::sts32f(stage + (uint32_t)(h0 + 1 - keep_lo) * 2048u + 4u * d, v[h + 1]);
+      } else {
+        const float mine = odd ? v[h + 1] : v[h];
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
+        const int hl = h0 + (odd ? 1 : 0);
+        if (hl < rows)
+          *reinterpret_cast<float2*>(dst + (size_t)hl * kDLatent + d0) =
+              odd ? make_float2(other, mine) : make_float2(mine, other);
       }
     }
   }
+}
+
+// Merge of the partitions inside the kernel ("The 64-Block Barrier", "The Split-K Prescription": the
+// partial results combined by an online-softmax merge), for a launch whose nsplit CTAs of one (query,
+// head group) form a thread-block cluster (rank = partition s).  CTA s owns the heads [s L, s L + L) of the
+// group, L = NH / nsplit:
+//   1. every CTA pushes its partition's lse of every head into every CTA's lse_all[s] (distributed shared
+//      memory), writes its normalised partial rows O_s / l_s of the other CTAs' heads into its partial rows
+//      of the workspace (fp32), and stages those of its own heads in shared memory; one cluster barrier
+//      (release / acquire) makes all of it visible;
+//   2. every CTA bulk-loads, for its own heads, the partial rows of every peer whose partition holds a
+//      valid entry (a partition is empty for all heads or for none), and writes
+//      out = sum_s exp(lse_s - lse) O_s / l_s (bf16) and lse = ln sum_s exp(lse_s) for them.
+// A partition with no valid entry, or whose CTA gave up a wait, counts as lse = -inf (weight 0); every
+// CTA takes the cluster barriers whatever happened, so no CTA waits on one that left.
+template <int NH>
+__device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bool own_ok) {
+  const SplitParams& p = *x.p;
+  Misc& ms = *x.ms;
+  const int S = p.nsplit, s = x.split, L = NH / S;
+  const uint32_t stage = x.k_base;            // own rows at 0, then one L-row block per peer
+  const int t = threadIdx.x;
+  // 1. (the split cluster barrier started at kernel start completes here: every peer's shared memory exists)
+  ptx::cluster_wait();
+  const bool own_rows = own_ok && ms.lse_out[0] != -CUDART_INF_F;
+  if (t < NH) {
+    const float l = own_ok ? ms.lse_out[t] : -CUDART_INF_F;
+    const uint32_t a = ptx::smem_u32(&ms.lse_all[s][t]);
+    for (int r = 0; r < S; ++r) ptx::st_cluster_f32(ptx::mapa(a, (uint32_t)r), l);
+  }
+  if (own_rows) {
+    float* part = p.o_part + (((size_t)x.b * S + s) * p.H + (size_t)x.g * NH) * kDLatent;
+    write_rows_f32<NH>(x, warp, lane, part, NH, stage, s * L, L);
+  }
+  ptx::cluster_sync_all();
+  // 2. the peers' rows of this CTA's heads
+  if (t == 0) {
+    ptx::fence_proxy_async_all();
+    uint32_t bytes = 0;
+    for (int r = 0; r < S; ++r)
+      if (r != s && ms.lse_all[r][0] != -CUDART_INF_F) bytes += (uint32_t)L * 2048u;
+    if (bytes) {
+      ptx::mbar_arrive_expect_tx(&ms.merge_in, bytes);
+      for (int r = 0, k = 1; r < S; ++r) {
+        if (r == s) continue;
+        if (ms.lse_all[r][0] != -CUDART_INF_F) {
+          const float* src = p.o_part + (((size_t)x.b * S + r) * p.H + (size_t)x.g * NH + (size_t)s * L) * kDLatent;
+          ptx::bulk_g2s(stage + (uint32_t)(k * L) * 2048u, src, (uint32_t)L * 2048u, &ms.merge_in);
+        }
+        ++k;
+      }
+    } else {
+      ptx::mbar_arrive(&ms.merge_in);
+    }
+  }
+  if (t < L) {
+    // merged lse and the weights of every partition for head s L + t
+    const int h = s * L + t;
+    float mx = -CUDART_INF_F;
+    for (int r = 0; r < S; ++r) mx = fmaxf(mx, ms.lse_all[r][h]);
+    float z = 0.f;
+    if (mx != -CUDART_INF_F)
+      for (int r = 0; r < S; ++r) z += expf(ms.lse_all[r][h] - mx);     // exp(-inf) = 0 for empty partitions
+    const float lse = mx == -CUDART_INF_F ? -CUDART_INF_F : mx + logf(z);
+    ms.lse_merged[t] = lse;
+    for (int r = 0; r < S; ++r)
+      ms.wts[r][t] = (lse == -CUDART_INF_F || ms.lse_all[r][h] == -CUDART_INF_F) ? 0.f : expf(ms.lse_all[r][h] - lse);
+  }
+  const bool in_ok = ptx::mbar_wait_bounded(&ms.merge_in, 0, x.abort, p.wait_ns);
+  const bool ok = __syncthreads_and(in_ok) != 0;
+  if (!ok) return;                           // flagged at teardown (abort)
+  uint16_t* out = p.out + ((size_t)x.b * p.H + (size_t)x.g * NH + (size_t)s * L) * kDLatent;
+  for (int id = t; id < L * (kDLatent / 4); id += kThreads) {
+    const int i = id / (kDLatent / 4), j = id % (kDLatent / 4);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int r = 0, k = 1; r < S; ++r) {
+      const float w = ms.wts[r][i];
+      const int blk = r == s ? 0 : k;
+      if (r != s) ++k;
+      if (w == 0.f) continue;                // an empty partition: its rows are not read
+      const float4 v = ptx::lds128f(stage + (uint32_t)(blk * L + i) * 2048u + 16u * j);
+      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+    }
+    reinterpret_cast<uint2*>(out + (size_t)i * kDLatent)[j] =
+        make_uint2(f32x2_to_bf16x2(acc.x, acc.y), f32x2_to_bf16x2(acc.z, acc.w));
+  }
+  if (t < L) p.lse[(size_t)x.b * p.H + (size_t)x.g * NH + (size_t)s * L + t] = ms.lse_merged[t];
 }
 
 template <int NH>
@@ -717,6 +859,26 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   x.hg_valid = min(NH, p.H - NH * x.g);
 
   if (x.n_tiles == 0) {
+    if (p.fused) {
+      // an empty partition still owns a head slice of the merge: weight 0 for its own rows
+      if (threadIdx.x == 0) {
+        ptx::mbar_init(&ms.merge_in, 1);
+        ms.abort = 0;
+        ptx::fence_mbar_init();
+      }
+      ptx::cluster_arrive_relaxed();
+      __syncthreads();
+      ptx::griddep_wait();
+      fused_merge<NH>(x, warp, lane, false);
+      if (threadIdx.x == 0 && ms.abort) {
+        // the merge's bulk loads into this CTA land before it leaves (time limit only)
+        volatile int no_abort = 0;
+        ptx::mbar_wait_bounded(&ms.merge_in, 0, &no_abort, 100000000ull);
+        if (p.err) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
+      }
+      __syncthreads();
+      return;
+    }
     // empty partition: out = 0, lse = -inf
     ptx::griddep_wait();
     for (int i = threadIdx.x; i < x.hg_valid * kDLatent; i += kThreads) {
@@ -743,6 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     ptx::mbar_init(&ms.pv0_done, 1);
     ptx::mbar_init(&ms.pv_done, 1);
     ptx::mbar_init(&ms.teardown, 1);
+    ptx::mbar_init(&ms.merge_in, 1);
     ms.abort = 0;
     ms.range_err = 0;
     ptx::fence_mbar_init();
@@ -756,6 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   __syncthreads();
   ptx::tc_fence_after();
   x.tmem = ms.tmem_slot;
+  if (p.fused) ptx::cluster_arrive_relaxed();   // waited for before the merge writes into the peers
   // launched as a programmatic dependent: the setup above overlapped the previous kernel's tail;
   // nothing in global memory (inputs it may have written, partials it may still read) is touched
   // before that kernel has completed
@@ -781,9 +945,21 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     ms.lse_out[h] = L > 0.f ? (ms.m_ref[h] + log2f(L)) * 0.6931471805599453f : -CUDART_INF_F;
   }
   __syncthreads();
-  const bool out_ok = ok && !ms.abort;
-  if (out_ok) {
-    epilogue_write<NH>(x, warp, lane);
+  const bool out_ok = ok && !ms.abort;      // the same for every thread (any failed wait set ms.abort)
+  if (p.fused) {
+    fused_merge<NH>(x, warp, lane, out_ok);
+  } else if (out_ok) {
+    if (p.final_out) {
+      // bf16 O / l staged as rows in the K tile, then bulk-stored (the head group's rows are contiguous)
+      stage_rows<NH, false>(x, warp, lane, x.k_base, ms.linv);
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+      store_rows(p.out + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDLatent, x.k_base, x.hg_valid, 1024u, warp, lane);
+    } else {
+      // fp32 partial rows straight from registers (measured faster than staging plus bulk stores here)
+      float* part = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + (size_t)x.g * NH) * kDLatent;
+      write_rows_f32<NH>(x, warp, lane, part, x.hg_valid, x.k_base, 0, 0);
+    }
     if ((int)threadIdx.x < x.hg_valid) {
       const int hl = threadIdx.x;
       const size_t h = (size_t)x.g * NH + hl;
@@ -804,6 +980,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
       // are waited for (time limit only) before the CTA leaves
       drained = ptx::mbar_wait_bounded(&ms.q_raw, 0, &no_abort, 100000000ull) && drained;
       drained = ptx::mbar_wait_bounded(&ms.raw0, 0, &no_abort, 100000000ull) && drained;
+      // the merge's bulk loads into this CTA (always armed in fused_merge) likewise
+      if (p.fused) drained = ptx::mbar_wait_bounded(&ms.merge_in, 0, &no_abort, 100000000ull) && drained;
     }
     if (p.err) {
       if (ms.abort || !drained) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
@@ -823,6 +1001,10 @@ bool split_shape_supported(int H, int topk) {
 bool split_heads_supported(int nh) { return nh == 16 || nh == 32 || nh == 64; }
 
 int split_ctas_per_unit() { return 1; }
+
+bool split_fusable(int nsplit, int nh, int H) {
+  return nsplit >= 2 && nsplit <= kMaxFusedSplit && nh % nsplit == 0 && nh <= H;
+}
 
 int split_ctas_per_sm(int H) {
   (void)H;
@@ -873,11 +1055,20 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem_bytes<NH>();
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (p.fused) {
+    // the partitions of a (query, head group) as one cluster: co-scheduled, they merge through each
+    // other's shared memory and the workspace
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)p.nsplit;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, split_kernel<NH>, p);
 }
 

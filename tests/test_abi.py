@@ -84,6 +84,20 @@ def test_noalloc_dims_statuses_match_the_workspace_entry_point(lib):
     assert lib.sparse_mla_noalloc_read_errors(None, None) == 1
 
 
+def test_merge_selector(lib):
+    d = make_dims(32, 64, 512, 16, 100, nsplit=4, merge=3)
+    assert _decode(lib, d) == 1                                        # no such merge mode
+    p = _native.SmlaPlan()
+    d = make_dims(32, 64, 512, 16, 100, nsplit=3, heads_per_cta=64, merge=2)
+    assert lib.sparse_mla_plan_for(C.byref(d), 152, C.byref(p)) == 2   # 3 partitions do not divide 64 heads
+    for merge, fused in ((1, 0), (2, 1)):
+        d = make_dims(32, 64, 512, 16, 100, nsplit=4, heads_per_cta=64, merge=merge)
+        assert lib.sparse_mla_plan_for(C.byref(d), 152, C.byref(p)) == 0 and p.fused == fused
+    d = make_dims(32, 64, 512, 16, 100, merge=2)                       # automatic split count, in-kernel merge
+    assert lib.sparse_mla_plan_for(C.byref(d), 152, C.byref(p)) == 0
+    assert p.nsplit == 1 or (p.fused == 1 and p.heads_per_cta % p.nsplit == 0 and p.nsplit <= 8)
+
+
 def test_debug_entry_points_host_checks(lib):
     d = make_dims(4, 64, 512, 16, 100, nsplit=4)
     assert lib.sparse_mla_decode_rows(C.byref(d), FAKE, FAKE, FAKE, FAKE, FAKE, C.c_float(0.04), FAKE, FAKE,

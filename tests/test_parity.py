@@ -67,6 +67,36 @@ def test_split_merge_heads_and_partitions(H, nsplit):
     compare(out, lse, *oracle_on(w))
 
 
+@pytest.mark.parametrize("merge", [api.MERGE_KERNEL, api.MERGE_FUSED])
+@pytest.mark.parametrize("H,nsplit,nh", [(64, 2, 64), (64, 4, 64), (64, 8, 64), (64, 4, 32), (32, 8, 16),
+                                         (16, 2, 16), (128, 4, 64)])
+def test_merge_kernel_and_in_kernel_merge(H, nsplit, nh, merge):
+    # the same partitions merged by the merge kernel or inside the split kernel (a cluster of the
+    # partitions): several tiles per partition, partitions made only of padding (ctx 40), a one-token
+    # context, duplicated entries
+    w = _custom(B=4, H=H, topk=480, ctx=[6000, 40, 1, 900], seed=60 + H + nsplit + nh, outlier_channels=2)
+    w.topk_idx[3, :4] = torch.tensor([3, 3, 3, 899], dtype=torch.int32, device=DEV)
+    out, lse = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                     nsplit=nsplit, heads_per_cta=nh, merge=merge)
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle_on(w))
+    assert torch.all(torch.isneginf(lse[2]) == False)      # noqa: E712  (one valid token: finite lse)
+
+
+def test_in_kernel_merge_rows_and_flags():
+    w = _custom(B=3, H=64, topk=512, ctx=[3000, 700, 5], seed=77)
+    w.block_table[0, 5] = w.num_pages + 1
+    dims = api.dims_of(w.q, w.kv_cache, w.block_table, w.topk_idx, 4, 64, api.MERGE_FUSED)
+    ws = api.alloc_workspace(dims, 4)
+    out, lse, rows = api.sparse_mla_decode_rows(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens,
+                                                w.sm_scale, workspace=ws, nsplit=4, heads_per_cta=64,
+                                                merge=api.MERGE_FUSED)
+    torch.cuda.synchronize()
+    assert api.read_errors(ws) == 0x1
+    assert np.array_equal(rows.cpu().numpy(), oracle_rows(w))
+    compare(out, lse, *oracle_on(w))
+
+
 @pytest.mark.parametrize("s_q,nsplit", [(2, 0), (3, 2), (4, 1)])
 def test_several_queries_per_request(s_q, nsplit):
     # the MTP / verify shape: s_q queries per request, each with its own top-k and causal length

@@ -14,17 +14,17 @@ from parity_util import compare, oracle_on
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("nsplit", [1, 2])
-def test_wait_that_runs_out_is_reported_and_recoverable(nsplit):
+@pytest.mark.parametrize("nsplit,merge", [(1, api.MERGE_AUTO), (2, api.MERGE_KERNEL), (2, api.MERGE_FUSED)])
+def test_wait_that_runs_out_is_reported_and_recoverable(nsplit, merge):
     w = wl.make_workload(wl.CONFIGS["tiny"], device="cuda")
-    dims = api.dims_of(w.q, w.kv_cache, w.block_table, w.topk_idx, nsplit)
+    dims = api.dims_of(w.q, w.kv_cache, w.block_table, w.topk_idx, nsplit, 0, merge)
     ws = api.alloc_workspace(dims, nsplit)
     out = torch.full((w.B, w.H, 512), 3.0, dtype=torch.bfloat16, device="cuda")
     lse = torch.full((w.B, w.H), 3.0, dtype=torch.float32, device="cuda")
     try:
         api.debug_set_wait_limit(1)
         api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale, out=out,
-                              lse=lse, workspace=ws, nsplit=nsplit)
+                              lse=lse, workspace=ws, nsplit=nsplit, merge=merge)
         torch.cuda.synchronize()                         # the call returns; no fault
     finally:
         api.debug_set_wait_limit(0)
@@ -33,7 +33,7 @@ def test_wait_that_runs_out_is_reported_and_recoverable(nsplit):
         assert torch.all(out == 3.0) and torch.all(lse == 3.0)
     api.clear_errors(ws)
     out2, lse2 = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
-                                       workspace=ws, nsplit=nsplit)
+                                       workspace=ws, nsplit=nsplit, merge=merge)
     torch.cuda.synchronize()
     assert api.read_errors(ws) == 0
     compare(out2, lse2, *oracle_on(w))
