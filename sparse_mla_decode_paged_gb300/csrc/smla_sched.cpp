@@ -15,24 +15,24 @@
 
 namespace smla {
 
-// Cost-model constants (microseconds) of the split kernel on GB300, fitted to its measured times, for
-// CTAs of 64, 32 and 16 heads: a fixed per-CTA latency (launch, index chain, Q and first record loads)
-// plus the epilogue (NH output rows), a per-tile cost with a part that scales with the top-k entries
-// of the tile (record loads and conversion, which bound a tile at every NH), the extra cost of fp32
-// partial rows over the bf16 output, and the merge kernel.  Fitted to graph-replay sweeps of every
-// (nsplit, NH) on the five workloads (model vs measured within ~15%).
+// Cost-model constants (microseconds) of the split kernel on GB300, for CTAs of 64, 32 and 16 heads: a
+// fixed per-CTA latency (launch, index chain, Q and first record loads) plus the epilogue (NH output
+// rows), a per-tile cost with a part that scales with the top-k entries of the tile, the extra cost of
+// fp32 partial rows over the bf16 output, the merge kernel, and the merge inside a cluster.  Fitted by
+// least squares on the relative error to graph-replay sweeps of every (nsplit, NH, merge path) on the
+// five workloads, 176 points: model / measured within 0.81 .. 1.08 (median 1.00).
 struct CostModel {
-  double cta_fixed_us = 8.3;
-  double epilogue_us_per_head = 3.6 / 64;
-  double tile_fixed_us[3] = {2.0, 2.3, 2.9};              // NH = 16, 32, 64
-  double tile_token_us[3] = {3.0 / 128, 3.0 / 128, 3.1 / 128};
-  double partial_extra_us_per_head = 0.7 / 64;         // fp32 partial rows instead of bf16 output
-  double combine_fixed_us = 2.0;       // merge kernel: launch (overlapped with the split kernel's tail)
-  double combine_gbs = 6000.0;
-  // merge inside a cluster: a fixed part (two cluster barriers, the lse exchange) plus the weighted fp32
-  // rows each CTA bulk-stores for its peers and bulk-loads from them, at a per-SM rate
-  double fused_fixed_us = 1.0;
-  double fused_bytes_per_us = 64e3;
+  double cta_fixed_us = 2.93;
+  double epilogue_us_per_head = 0.0607;
+  double tile_fixed_us[3] = {5.52, 5.67, 6.05};           // NH = 16, 32, 64
+  double tile_token_us[3] = {0.00564, 0.00981, 0.00652};
+  double partial_extra_us_per_head = 0.0134;           // fp32 partial rows instead of bf16 output
+  double combine_fixed_us = 2.26;      // merge kernel: launch (overlapped with the split kernel's tail)
+  double combine_gbs = 4550.0;
+  // merge inside a cluster: a fixed part (the cluster barrier, the lse exchange) plus the fp32 rows each
+  // CTA stores for its peers and bulk-loads from them, at a per-SM rate
+  double fused_fixed_us = 2.54;
+  double fused_bytes_per_us = 54800.0;
 };
 
 // Clusters of `csize` CTAs (one CTA per SM) that fit at once: the SMs of a GPC that a cluster size does not
