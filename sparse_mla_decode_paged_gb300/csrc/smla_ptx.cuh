@@ -148,6 +148,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Orders this thread's accesses through the async proxy (bulk copies) and the generic proxy in every
 // state space: after a completed bulk store, before a release; after an acquire, before a bulk load.
 __device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+// The same for the global state space only.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Named barrier over `threads` threads (non-aligned form: lanes of a warp may arrive separately).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads) {
@@ -351,6 +353,12 @@ __device__ __forceinline__ float4 lds128f(uint32_t saddr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(saddr)
                : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds64(uint32_t saddr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(saddr) : "memory");
   return v;
 }
 

@@ -697,14 +697,14 @@ __device__ __forceinline__ void store_rows(void* dst, uint32_t stage, int rows, 
   }
 }
 
-// O / l in fp32 from TMEM: rows of heads outside [keep_lo, keep_lo + keep_n) go straight to global
-// memory at dst (row h at dst + h * 512), rows inside it are staged in shared memory at `stage` (row h -
-// keep_lo, 2048 bytes each).  Warp w reads TMEM lane quadrant w % 4 and the column chunks w / 4, w / 4 + 3,
-// ... of O^T (as stage_rows); lanes 2j, 2j + 1 hold dims d, d + 1 and exchange one value per head pair, so
-// each global store writes two dims of one row (a warp's store covers two rows of 64 bytes).
-template <int NH>
-__device__ __forceinline__ void write_rows_f32(const Ctx& x, int warp, int lane, float* dst, int rows,
-                                               uint32_t stage, int keep_lo, int keep_n) {
+// O / l from TMEM: rows of heads outside [keep_lo, keep_lo + keep_n) go straight to global memory at dst
+// (row h at dst + h * 512 elements: fp32, or fp16 when kHalf), rows inside it are staged in fp32 in shared
+// memory at `stage` (row h - keep_lo, 2048 bytes each).  Warp w reads TMEM lane quadrant w % 4 and the
+// column chunks w / 4, w / 4 + 3, ... of O^T (as stage_rows); lanes 2j, 2j + 1 hold dims d, d + 1 and
+// exchange one value per head pair, so each global store writes two dims of one row.
+template <int NH, bool kHalf>
+__device__ __forceinline__ void write_rows(const Ctx& x, int warp, int lane, void* dst, int rows, uint32_t stage,
+                                           int keep_lo, int keep_n) {
   using C = Cfg<NH>;
   constexpr int kCols = C::kChunkCols;
   const Misc& ms = *x.ms;
@@ -738,9 +738,14 @@ __device__ __forceinline__ void write_rows_f32(const Ctx& x, int warp, int lane,
         const float mine = odd ? v[h + 1] : v[h];
         const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
         const int hl = h0 + (odd ? 1 : 0);
-        if (hl < rows)
-          *reinterpret_cast<float2*>(dst + (size_t)hl * kDLatent + d0) =
-              odd ? make_float2(other, mine) : make_float2(mine, other);
+        const float lo = odd ? other : mine, hi = odd ? mine : other;   // dims d0, d0 + 1
+        if (hl < rows) {
+          if constexpr (kHalf)
+            *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(dst) + (size_t)hl * kDLatent + d0) =
+                f32x2_to_f16x2_sat(lo, hi);
+          else
+            *reinterpret_cast<float2*>(static_cast<float*>(dst) + (size_t)hl * kDLatent + d0) = make_float2(lo, hi);
+        }
       }
     }
   }
@@ -751,9 +756,11 @@ __device__ __forceinline__ void write_rows_f32(const Ctx& x, int warp, int lane,
 // head group) form a thread-block cluster (rank = partition s).  CTA s owns the heads [s L, s L + L) of the
 // group, L = NH / nsplit:
 //   1. every CTA pushes its partition's lse of every head into every CTA's lse_all[s] (distributed shared
-//      memory), writes its normalised partial rows O_s / l_s of the other CTAs' heads into its partial rows
-//      of the workspace (fp32), and stages those of its own heads in shared memory; one cluster barrier
-//      (release / acquire) makes all of it visible;
+//      memory), writes its normalised partial rows O_s / l_s of the other CTAs' heads into the workspace in
+//      fp16 (a convex combination of dequantised latents, which stay inside the fp16 range; the rounding is
+//      2^-11 relative against the 5e-3 output tolerance, and halves the exchange that bounds this step),
+//      and stages those of its own heads in fp32 in shared memory; one cluster barrier (release / acquire)
+//      makes all of it visible;
 //   2. every CTA bulk-loads, for its own heads, the partial rows of every peer whose partition holds a
 //      valid entry (a partition is empty for all heads or for none), and writes
 //      out = sum_s exp(lse_s - lse) O_s / l_s (bf16) and lse = ln sum_s exp(lse_s) for them.
@@ -774,24 +781,26 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
     const uint32_t a = ptx::smem_u32(&ms.lse_all[s][t]);
     for (int r = 0; r < S; ++r) ptx::st_cluster_f32(ptx::mapa(a, (uint32_t)r), l);
   }
-  if (own_rows) {
-    float* part = p.o_part + (((size_t)x.b * S + s) * p.H + (size_t)x.g * NH) * kDLatent;
-    write_rows_f32<NH>(x, warp, lane, part, NH, stage, s * L, L);
-  }
+  // the fp16 rows of partition r: [B][nsplit][H][512] fp16 in the workspace's partial area
+  uint16_t* part16 = reinterpret_cast<uint16_t*>(p.o_part);
+  if (own_rows)
+    write_rows<NH, true>(x, warp, lane, part16 + (((size_t)x.b * S + s) * p.H + (size_t)x.g * NH) * kDLatent, NH,
+                         stage, s * L, L);
   ptx::cluster_sync_all();
-  // 2. the peers' rows of this CTA's heads
+  // 2. the peers' rows of this CTA's heads (fp16, after the own fp32 rows)
+  const uint32_t peers = stage + (uint32_t)L * 2048u;
   if (t == 0) {
-    ptx::fence_proxy_async_all();
+    ptx::fence_proxy_async_global();
     uint32_t bytes = 0;
     for (int r = 0; r < S; ++r)
-      if (r != s && ms.lse_all[r][0] != -CUDART_INF_F) bytes += (uint32_t)L * 2048u;
+      if (r != s && ms.lse_all[r][0] != -CUDART_INF_F) bytes += (uint32_t)L * 1024u;
     if (bytes) {
       ptx::mbar_arrive_expect_tx(&ms.merge_in, bytes);
-      for (int r = 0, k = 1; r < S; ++r) {
+      for (int r = 0, k = 0; r < S; ++r) {
         if (r == s) continue;
         if (ms.lse_all[r][0] != -CUDART_INF_F) {
-          const float* src = p.o_part + (((size_t)x.b * S + r) * p.H + (size_t)x.g * NH + (size_t)s * L) * kDLatent;
-          ptx::bulk_g2s(stage + (uint32_t)(k * L) * 2048u, src, (uint32_t)L * 2048u, &ms.merge_in);
+          const uint16_t* src = part16 + (((size_t)x.b * S + r) * p.H + (size_t)x.g * NH + (size_t)s * L) * kDLatent;
+          ptx::bulk_g2s(peers + (uint32_t)(k * L) * 1024u, src, (uint32_t)L * 1024u, &ms.merge_in);
         }
         ++k;
       }
@@ -819,12 +828,20 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
   for (int id = t; id < L * (kDLatent / 4); id += kThreads) {
     const int i = id / (kDLatent / 4), j = id % (kDLatent / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int r = 0, k = 1; r < S; ++r) {
+    for (int r = 0, k = 0; r < S; ++r) {
       const float w = ms.wts[r][i];
-      const int blk = r == s ? 0 : k;
-      if (r != s) ++k;
-      if (w == 0.f) continue;                // an empty partition: its rows are not read
-      const float4 v = ptx::lds128f(stage + (uint32_t)(blk * L + i) * 2048u + 16u * j);
+      float4 v;
+      if (r == s) {
+        if (w == 0.f) continue;              // an empty partition: its rows are not read
+        v = ptx::lds128f(stage + (uint32_t)i * 2048u + 16u * j);
+      } else {
+        const uint32_t row = peers + (uint32_t)(k * L + i) * 1024u;
+        ++k;
+        if (w == 0.f) continue;
+        const uint2 hv = ptx::lds64(row + 8u * j);
+        const float2 a = f16x2_to_f32x2(hv.x), b2 = f16x2_to_f32x2(hv.y);
+        v = make_float4(a.x, a.y, b2.x, b2.y);
+      }
       acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
     }
@@ -958,7 +975,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     } else {
       // fp32 partial rows straight from registers (measured faster than staging plus bulk stores here)
       float* part = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + (size_t)x.g * NH) * kDLatent;
-      write_rows_f32<NH>(x, warp, lane, part, x.hg_valid, x.k_base, 0, 0);
+      write_rows<NH, false>(x, warp, lane, part, x.hg_valid, x.k_base, 0, 0);
     }
     if ((int)threadIdx.x < x.hg_valid) {
       const int hl = threadIdx.x;
