@@ -727,6 +727,8 @@ def main():
     ap.add_argument("--single", type=int, default=0,
                     help="profiling driver: run this many eager calls of --workload (optionally --nsplit) and exit")
     ap.add_argument("--nsplit", type=int, default=0)
+    ap.add_argument("--ctx", type=int, default=0,
+                    help="with --single: context length per query instead of the workload's (ragged: the upper end)")
     ap.add_argument("--single-op", choices=("decode", "topk"), default="decode",
                     help="with --single: the decode call, or the top-k selection over the workload's contexts")
     args = ap.parse_args()
@@ -741,10 +743,17 @@ def main():
         torch.cuda.synchronize()
         return
     if args.single:
+        import dataclasses
         import torch
         from sparse_mla_decode_paged_gb300 import api
         from sparse_mla_decode_paged_gb300 import workloads as wl
-        w = wl.make_workload(wl.CONFIGS[args.workload], device="cuda")
+        spec = wl.CONFIGS[args.workload]
+        if args.ctx:
+            # the same batch, heads and top-k list length over shorter contexts: the kernels do the same work
+            # per query, the cache holds only the pages used (a few GB at most, for profiling)
+            spec = (dataclasses.replace(spec, ragged_hi=args.ctx, pool_pages=None) if spec.ctx is None
+                    else dataclasses.replace(spec, ctx=args.ctx, pool_pages=None))
+        w = wl.make_workload(spec, device="cuda")
         for _ in range(args.single):
             api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
                                   nsplit=args.nsplit)

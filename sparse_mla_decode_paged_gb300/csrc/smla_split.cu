@@ -647,18 +647,21 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 }
 
 // ------------------------------------------------------------------------------------------ epilogue
-// O^T from TMEM, scaled per head by scale[h] (1/l, or the merge weight of this partition), staged as rows
-// [head][512] at `stage` (the K tile, free once every PV MMA has completed): fp32 rows of 2048 bytes or
-// bf16 rows of 1024 bytes.  Warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim
-// block) and the column chunks w / 4, w / 4 + 3, ... of O^T (chunks of 32 columns, 16 for NH = 16; block
-// c * cols / NH); lane l writes dim d of every head of the chunk, so a warp's store covers 32
-// consecutive dims of one row.
-template <int NH, bool kF32>
-__device__ __forceinline__ void stage_rows(const Ctx& x, int warp, int lane, uint32_t stage, const float* scale) {
+// All 12 warps write O / l from TMEM straight to the output rows [head][512] (bf16, or fp32
+// partials): warp w reads TMEM lane quadrant w % 4 (dims 32 (w % 4) .. of each 128-dim block) and the
+// column chunks c = w / 4, w / 4 + 3, ... of O^T (chunks of 32 columns, 16 for NH = 16; block
+// c * cols / NH).  Lanes 2j, 2j + 1 hold dims d, d + 1; for heads h, h + 1 the even lane writes row h
+// and the odd lane row h + 1, two dims each.
+template <int NH>
+__device__ __forceinline__ void epilogue_write(const Ctx& x, int warp, int lane) {
   using C = Cfg<NH>;
   constexpr int kCols = C::kChunkCols;
+  const SplitParams& p = *x.p;
+  Misc& ms = *x.ms;
   const int quad = warp & 3;
   const uint32_t lane_q = (uint32_t)(32 * quad) << 16;
+  const bool odd = lane & 1;
+  const size_t head0 = (size_t)x.g * NH;
 #pragma unroll 1
   for (int c = warp >> 2; c < C::kChunks; c += 3) {
     const int jb = (kCols * c) / NH, hb = (kCols * c) % NH;
@@ -668,39 +671,36 @@ __device__ __forceinline__ void stage_rows(const Ctx& x, int warp, int lane, uin
     float v[kCols];
 #pragma unroll
     for (int k = 0; k < kCols / 4; ++k) {
-      const float4 l4 = reinterpret_cast<const float4*>(scale + hb)[k];
+      const float4 l4 = reinterpret_cast<const float4*>(ms.linv + hb)[k];
       v[4 * k] = l4.x; v[4 * k + 1] = l4.y; v[4 * k + 2] = l4.z; v[4 * k + 3] = l4.w;
     }
     ptx::tmem_wait_ld();
-    const uint32_t d = 128 * jb + 32 * quad + lane;
 #pragma unroll
-    for (int h = 0; h < kCols; ++h) {
-      const float o = v[h] * __uint_as_float(r[h]);
-      if constexpr (kF32) ptx::sts32f(stage + (uint32_t)(hb + h) * 2048u + 4u * d, o);
-      else ptx::sts16(stage + (uint32_t)(hb + h) * 1024u + 2u * d, (uint16_t)(f32x2_to_bf16x2(o, 0.f) & 0xFFFFu));
+    for (int h = 0; h < kCols; ++h) v[h] *= __uint_as_float(r[h]);
+    const int d0 = 128 * jb + 32 * quad + (lane & ~1);
+#pragma unroll
+    for (int h = 0; h < kCols; h += 2) {
+      const float mine = odd ? v[h + 1] : v[h];
+      const float other = __shfl_xor_sync(0xffffffffu, odd ? v[h] : v[h + 1], 1);
+      const float lo = odd ? other : mine, hi = odd ? mine : other;   // dims d0, d0 + 1
+      const int hl = hb + h + (odd ? 1 : 0);
+      if (hl < x.hg_valid) {
+        if (p.final_out) {
+          uint16_t* dst = p.out + ((size_t)x.b * p.H + head0 + hl) * kDLatent + d0;
+          *reinterpret_cast<uint32_t*>(dst) = f32x2_to_bf16x2(lo, hi);
+        } else {
+          float* dst = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + head0 + hl) * kDLatent + d0;
+          *reinterpret_cast<float2*>(dst) = make_float2(lo, hi);
+        }
+      }
     }
-  }
-}
-
-// Rows [0, rows) of `row_bytes` each, staged contiguously at `stage`, to contiguous global rows at dst: the
-// lanes of warp 0 each bulk-copy four rows, then wait until the copies have read shared memory (the
-// global writes complete before the grid does).  Call after a proxy fence and a CTA barrier.
-__device__ __forceinline__ void store_rows(void* dst, uint32_t stage, int rows, uint32_t row_bytes, int warp, int lane) {
-  if (warp != 0) return;
-  const int r0 = 4 * lane;
-  if (r0 < rows) {
-    const int n = min(4, rows - r0);
-    ptx::bulk_s2g(static_cast<unsigned char*>(dst) + (size_t)r0 * row_bytes, stage + (uint32_t)r0 * row_bytes,
-                  (uint32_t)n * row_bytes);
-    ptx::bulk_commit();
-    ptx::bulk_wait_read_all();
   }
 }
 
 // O / l from TMEM: rows of heads outside [keep_lo, keep_lo + keep_n) go straight to global memory at dst
 // (row h at dst + h * 512 elements: fp32, or fp16 when kHalf), rows inside it are staged in fp32 in shared
 // memory at `stage` (row h - keep_lo, 2048 bytes each).  Warp w reads TMEM lane quadrant w % 4 and the
-// column chunks w / 4, w / 4 + 3, ... of O^T (as stage_rows); lanes 2j, 2j + 1 hold dims d, d + 1 and
+// column chunks w / 4, w / 4 + 3, ... of O^T (as epilogue_write); lanes 2j, 2j + 1 hold dims d, d + 1 and
 // exchange one value per head pair, so each global store writes two dims of one row.
 template <int NH, bool kHalf>
 __device__ __forceinline__ void write_rows(const Ctx& x, int warp, int lane, void* dst, int rows, uint32_t stage,
@@ -851,7 +851,9 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
   if (t < L) p.lse[(size_t)x.b * p.H + (size_t)x.g * NH + (size_t)s * L + t] = ms.lse_merged[t];
 }
 
-template <int NH>
+// kFused: the partitions of a (query, head group) form a cluster and merge inside the kernel; a separate
+// instantiation, so that the other launches carry none of that code.
+template <int NH, bool kFused>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p) {
   using C = Cfg<NH>;
   extern __shared__ unsigned char smem_raw[];
@@ -876,7 +878,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   x.hg_valid = min(NH, p.H - NH * x.g);
 
   if (x.n_tiles == 0) {
-    if (p.fused) {
+    if constexpr (kFused) {
       // an empty partition still owns a head slice of the merge: weight 0 for its own rows
       if (threadIdx.x == 0) {
         ptx::mbar_init(&ms.merge_in, 1);
@@ -936,7 +938,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   __syncthreads();
   ptx::tc_fence_after();
   x.tmem = ms.tmem_slot;
-  if (p.fused) ptx::cluster_arrive_relaxed();   // waited for before the merge writes into the peers
+  if constexpr (kFused) ptx::cluster_arrive_relaxed();   // waited for before the merge writes into the peers
   // launched as a programmatic dependent: the setup above overlapped the previous kernel's tail;
   // nothing in global memory (inputs it may have written, partials it may still read) is touched
   // before that kernel has completed
@@ -963,20 +965,10 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
   }
   __syncthreads();
   const bool out_ok = ok && !ms.abort;      // the same for every thread (any failed wait set ms.abort)
-  if (p.fused) {
+  if constexpr (kFused) {
     fused_merge<NH>(x, warp, lane, out_ok);
   } else if (out_ok) {
-    if (p.final_out) {
-      // bf16 O / l staged as rows in the K tile, then bulk-stored (the head group's rows are contiguous)
-      stage_rows<NH, false>(x, warp, lane, x.k_base, ms.linv);
-      ptx::fence_proxy_async_smem();
-      __syncthreads();
-      store_rows(p.out + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDLatent, x.k_base, x.hg_valid, 1024u, warp, lane);
-    } else {
-      // fp32 partial rows straight from registers (measured faster than staging plus bulk stores here)
-      float* part = p.o_part + (((size_t)x.b * p.nsplit + x.split) * p.H + (size_t)x.g * NH) * kDLatent;
-      write_rows<NH, false>(x, warp, lane, part, x.hg_valid, x.k_base, 0, 0);
-    }
+    epilogue_write<NH>(x, warp, lane);
     if ((int)threadIdx.x < x.hg_valid) {
       const int hl = threadIdx.x;
       const size_t h = (size_t)x.g * NH + hl;
@@ -998,7 +990,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
       drained = ptx::mbar_wait_bounded(&ms.q_raw, 0, &no_abort, 100000000ull) && drained;
       drained = ptx::mbar_wait_bounded(&ms.raw0, 0, &no_abort, 100000000ull) && drained;
       // the merge's bulk loads into this CTA (always armed in fused_merge) likewise
-      if (p.fused) drained = ptx::mbar_wait_bounded(&ms.merge_in, 0, &no_abort, 100000000ull) && drained;
+      if constexpr (kFused) drained = ptx::mbar_wait_bounded(&ms.merge_in, 0, &no_abort, 100000000ull) && drained;
     }
     if (p.err) {
       if (ms.abort || !drained) atomicOr(p.err, SMLA_DEVERR_TIMEOUT);
@@ -1032,9 +1024,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Kernel attributes of split_kernel<NH> on the current device: set once per device (a per-device flag,
+// Kernel attributes of split_kernel<NH, kFused> on the current device: set once per device (a per-device flag,
 // read without a lock once set; the first call on a device configures it under the lock).
-template <int NH>
+template <int NH, bool kFused>
 cudaError_t configure_split_nh(int dev) {
   static std::atomic<bool> configured[kMaxDevices];
   static std::mutex mu;
@@ -1042,7 +1034,7 @@ cudaError_t configure_split_nh(int dev) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_relaxed)) return cudaSuccess;
   cudaError_t e =
-      cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
+      cudaFuncSetAttribute(split_kernel<NH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
   if (e != cudaSuccess) return e;
   // the smallest shared-memory carveout that holds the CTA: the rest of the SM's SRAM is L1, where the
   // record loads in flight land (about 28 KB at 64 heads per CTA, 60 KB at 16 or 32)
@@ -1050,7 +1042,8 @@ cudaError_t configure_split_nh(int dev) {
   e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
   const int pct = (int)((100 * (smem_bytes<NH>() + 1024) + max_smem - 1) / max_smem);
-  e = cudaFuncSetAttribute(split_kernel<NH>, cudaFuncAttributePreferredSharedMemoryCarveout, pct < 100 ? pct : 100);
+  e = cudaFuncSetAttribute(split_kernel<NH, kFused>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           pct < 100 ? pct : 100);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
   return cudaSuccess;
@@ -1061,7 +1054,7 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = configure_split_nh<NH>(dev);
+  e = p.fused ? configure_split_nh<NH, true>(dev) : configure_split_nh<NH, false>(dev);
   if (e != cudaSuccess) return e;
   const int head_groups = (p.H + NH - 1) / NH;
   dim3 grid(p.nsplit, head_groups, p.B);
@@ -1086,7 +1079,7 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, split_kernel<NH>, p);
+  return p.fused ? cudaLaunchKernelEx(&cfg, split_kernel<NH, true>, p) : cudaLaunchKernelEx(&cfg, split_kernel<NH, false>, p);
 }
 
 }  // namespace
