@@ -62,7 +62,7 @@ constexpr uint64_t kShortWaitNs = 100000ull;
 // `limit_ns` or as soon as *abort is set; returns false then (and sets *abort).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int* abort,
                                                   uint64_t limit_ns = 1000000000ull) {
-  if (limit_ns < kShortWaitNs) {
+  if (__builtin_expect(limit_ns < kShortWaitNs, 0)) {
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
       if (mbar_test_wait(bar, parity)) return true;
