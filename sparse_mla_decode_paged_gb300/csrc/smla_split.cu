@@ -92,9 +92,10 @@ struct Misc {
   float lse_out[kHeadsMax];
   // merge inside a cluster of the query's partitions
   uint64_t merge_in;                     // peers' weighted rows of this CTA's head slice landed
-  alignas(16) float lse_all[kMaxFusedSplit][kHeadsMax];   // every partition's lse (pushed by each CTA)
-  alignas(16) float wts[kMaxFusedSplit][kHeadsMax / 2];   // merge weights of this CTA's heads (at most NH / 2)
-  alignas(16) float lse_merged[kHeadsMax / 2];
+  // (shared memory here is taken from the L1 that lands the record loads: kept small)
+  alignas(16) float lse_in[kHeadsMax];   // lse of this CTA's L heads in every partition r: [r * L + i]
+  alignas(16) float wts[kHeadsMax];      // merge weight of partition r for head i of this CTA: [r * L + i]
+  float lse_merged[kHeadsMax / 2];
 };
 
 template <int NH>
@@ -755,8 +756,8 @@ __device__ __forceinline__ void write_rows(const Ctx& x, int warp, int lane, voi
 // partial results combined by an online-softmax merge), for a launch whose nsplit CTAs of one (query,
 // head group) form a thread-block cluster (rank = partition s).  CTA s owns the heads [s L, s L + L) of the
 // group, L = NH / nsplit:
-//   1. every CTA pushes its partition's lse of every head into every CTA's lse_all[s] (distributed shared
-//      memory), writes its normalised partial rows O_s / l_s of the other CTAs' heads into the workspace in
+//   1. every CTA pushes its partition's lse of each head into the CTA that owns the head (distributed
+//      shared memory), writes its normalised partial rows O_s / l_s of the other CTAs' heads into the workspace in
 //      fp16 (a convex combination of dequantised latents, which stay inside the fp16 range; the rounding is
 //      2^-11 relative against the 5e-3 output tolerance, and halves the exchange that bounds this step),
 //      and stages those of its own heads in fp32 in shared memory; one cluster barrier (release / acquire)
@@ -778,8 +779,8 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
   const bool own_rows = own_ok && ms.lse_out[0] != -CUDART_INF_F;
   if (t < NH) {
     const float l = own_ok ? ms.lse_out[t] : -CUDART_INF_F;
-    const uint32_t a = ptx::smem_u32(&ms.lse_all[s][t]);
-    for (int r = 0; r < S; ++r) ptx::st_cluster_f32(ptx::mapa(a, (uint32_t)r), l);
+    const int r = t / L, i = t % L;          // owner of head t and its index there
+    ptx::st_cluster_f32(ptx::mapa(ptx::smem_u32(&ms.lse_in[s * L + i]), (uint32_t)r), l);
   }
   // the fp16 rows of partition r: [B][nsplit][H][512] fp16 in the workspace's partial area
   uint16_t* part16 = reinterpret_cast<uint16_t*>(p.o_part);
@@ -793,12 +794,12 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
     ptx::fence_proxy_async_global();
     uint32_t bytes = 0;
     for (int r = 0; r < S; ++r)
-      if (r != s && ms.lse_all[r][0] != -CUDART_INF_F) bytes += (uint32_t)L * 1024u;
+      if (r != s && ms.lse_in[r * L] != -CUDART_INF_F) bytes += (uint32_t)L * 1024u;
     if (bytes) {
       ptx::mbar_arrive_expect_tx(&ms.merge_in, bytes);
       for (int r = 0, k = 0; r < S; ++r) {
         if (r == s) continue;
-        if (ms.lse_all[r][0] != -CUDART_INF_F) {
+        if (ms.lse_in[r * L] != -CUDART_INF_F) {
           const uint16_t* src = part16 + (((size_t)x.b * S + r) * p.H + (size_t)x.g * NH + (size_t)s * L) * kDLatent;
           ptx::bulk_g2s(peers + (uint32_t)(k * L) * 1024u, src, (uint32_t)L * 1024u, &ms.merge_in);
         }
@@ -810,16 +811,17 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
   }
   if (t < L) {
     // merged lse and the weights of every partition for head s L + t
-    const int h = s * L + t;
     float mx = -CUDART_INF_F;
-    for (int r = 0; r < S; ++r) mx = fmaxf(mx, ms.lse_all[r][h]);
+    for (int r = 0; r < S; ++r) mx = fmaxf(mx, ms.lse_in[r * L + t]);
     float z = 0.f;
     if (mx != -CUDART_INF_F)
-      for (int r = 0; r < S; ++r) z += expf(ms.lse_all[r][h] - mx);     // exp(-inf) = 0 for empty partitions
+      for (int r = 0; r < S; ++r) z += expf(ms.lse_in[r * L + t] - mx);   // exp(-inf) = 0 for empty partitions
     const float lse = mx == -CUDART_INF_F ? -CUDART_INF_F : mx + logf(z);
     ms.lse_merged[t] = lse;
-    for (int r = 0; r < S; ++r)
-      ms.wts[r][t] = (lse == -CUDART_INF_F || ms.lse_all[r][h] == -CUDART_INF_F) ? 0.f : expf(ms.lse_all[r][h] - lse);
+    for (int r = 0; r < S; ++r) {
+      const float l = ms.lse_in[r * L + t];
+      ms.wts[r * L + t] = (lse == -CUDART_INF_F || l == -CUDART_INF_F) ? 0.f : expf(l - lse);
+    }
   }
   const bool in_ok = ptx::mbar_wait_bounded(&ms.merge_in, 0, x.abort, p.wait_ns);
   const bool ok = __syncthreads_and(in_ok) != 0;
@@ -829,7 +831,7 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
     const int i = id / (kDLatent / 4), j = id % (kDLatent / 4);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int r = 0, k = 0; r < S; ++r) {
-      const float w = ms.wts[r][i];
+      const float w = ms.wts[r * L + i];
       float4 v;
       if (r == s) {
         if (w == 0.f) continue;              // an empty partition: its rows are not read
