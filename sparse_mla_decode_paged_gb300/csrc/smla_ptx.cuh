@@ -123,6 +123,9 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
 // Split cluster barrier: every thread arrives once (relaxed: no ordering of earlier accesses) and later
 // waits; used to know that every CTA of the cluster has started before its shared memory is written.
 __device__ __forceinline__ void cluster_arrive_relaxed() { asm volatile("barrier.cluster.arrive.relaxed;" ::: "memory"); }
+// The same with release semantics: this thread's earlier accesses are visible to the cluster's threads
+// once their wait returns.
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Every thread of every CTA of the cluster (non-aligned forms).
@@ -145,10 +148,8 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Orders this thread's accesses through the async proxy (bulk copies) and the generic proxy in every
-// state space: after a completed bulk store, before a release; after an acquire, before a bulk load.
-__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
-// The same for the global state space only.
+// Orders this thread's accesses to global memory through the generic proxy with its later accesses
+// through the async proxy (bulk copies): after an acquire, before a bulk load of data other threads wrote.
 __device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Named barrier over `threads` threads (non-aligned form: lanes of a warp may arrive separately).
@@ -303,18 +304,6 @@ __device__ __forceinline__ int ldg_i32_now(const int32_t* p) {
   return v;
 }
 
-// Bulk copy (TMA engine) of `bytes` from this CTA's shared memory to global memory, tracked by the
-// issuing thread's bulk groups.  Both addresses 16-byte aligned, bytes a multiple of 16.
-__device__ __forceinline__ void bulk_s2g(void* gdst, uint32_t ssrc, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst), "r"(ssrc), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has finished reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until every committed bulk group of this thread has completed (its global writes performed).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Programmatic dependent launch: a grid launched with programmatic stream serialization after this
 // one may start once every CTA here has signalled (or exited); it waits for this grid's completion
 // and memory with griddep_wait before touching its results.
@@ -343,10 +332,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 __device__ __forceinline__ void sts32f(uint32_t saddr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(saddr), "f"(v) : "memory");
-}
-
-__device__ __forceinline__ void sts16(uint32_t saddr, uint16_t v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(saddr), "h"(v) : "memory");
 }
 
 __device__ __forceinline__ float4 lds128f(uint32_t saddr) {

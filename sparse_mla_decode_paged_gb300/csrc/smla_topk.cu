@@ -21,6 +21,9 @@
 // per-CTA bases) writes the kept positions in position order.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "smla_internal.h"
 #include "smla_ptx.cuh"
 
@@ -104,8 +107,6 @@ __device__ __forceinline__ void st_cluster_u32(uint32_t saddr, uint32_t rank, ui
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(saddr, rank)), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
 
 // Adds the active lanes' bins to histogram h (this CTA's shared memory); the lanes sharing the first
 // active lane's bin add with one atomic (a tie-heavy row puts whole warps in one bin).  Every lane of
@@ -225,7 +226,7 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
   }
   // the cluster's sums are zero everywhere before any CTA pushes into them; the barrier completes
   // while the chunk loads
-  if (csize > 1) cluster_arrive();
+  if (csize > 1) cluster_arrive_release();
   __syncthreads();
 
   // load the chunk as order keys, with the coarse histogram
@@ -523,20 +524,32 @@ bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csi
   return true;
 }
 
+constexpr int kMaxDevices = 64;
+
+// Kernel attributes of topk_kernel on the current device: set once per device (a per-device flag, read
+// without a lock once set; the first call on a device configures it under the lock).
+cudaError_t configure_topk(int dev) {
+  static std::atomic<bool> configured[kMaxDevices];
+  static std::mutex mu;
+  if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_relaxed)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)topk_smem_bytes(kTopkMaxChunk));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
+  return cudaSuccess;
+}
+
 cudaError_t launch_topk(const TopkParams& p, int batch, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
-  static int configured_device = -1;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_device != dev) {
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)topk_smem_bytes(kTopkMaxChunk));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-    configured_device = dev;
-  }
+  e = configure_topk(dev);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * p.csize));
   cfg.blockDim = dim3(kTkThreads);
