@@ -86,7 +86,7 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-SPLIT_KERNEL_SOURCES = ("smla_split.cu", "smla_ptx.cuh", "smla_device.cuh")
+SPLIT_KERNEL_SOURCES = ("smla_split.cu", "smla_split_layout.cuh", "smla_ptx.cuh", "smla_device.cuh")
 
 
 def kernel_source_hash() -> str:
