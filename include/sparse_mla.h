@@ -240,7 +240,7 @@ int sparse_mla_kv_append(const smla_append_dims* dims, const void* latent, const
 /* Shapes of one top-k selection call. */
 typedef struct smla_topk_dims {
   int32_t batch;          /* queries (rows of scores), >= 0                               */
-  int32_t num_cols;       /* scored positions per row, 1 .. 786432                        */
+  int32_t num_cols;       /* scored positions per row, 1 .. 1048576                       */
   int64_t row_stride;     /* elements between consecutive rows of scores, >= num_cols     */
   int32_t k;              /* positions kept per query, 1 .. 2048                           */
   int32_t cluster_ctas;   /* CTAs per row: 0 = chosen by the library, else 1 .. 16         */
@@ -261,19 +261,22 @@ typedef struct smla_topk_dims {
  *   seq_lens int32 [batch]; topk_idx int32 [batch][k] (written)
  *   err_word device uint32 (may be NULL).
  * Returns SMLA_ERR_INVALID_ARG for null or misaligned pointers and bad
- * shapes, SMLA_ERR_UNSUPPORTED for num_cols > 786432 or k > 2048 (or a fixed
- * cluster_ctas whose chunk exceeds 49152 positions), SMLA_ERR_CUDA if the
+ * shapes, SMLA_ERR_UNSUPPORTED for num_cols > 1048576 or k > 2048 (or a fixed
+ * cluster_ctas whose chunk exceeds 65536 positions), SMLA_ERR_CUDA if the
  * launch fails (clusters of more than 8 CTAs, used only for rows longer than
- * 393216 positions, need the device to co-schedule them).  Asynchronous on
+ * 524288 positions, need the device to co-schedule them).  Asynchronous on
  * `stream`. */
 int sparse_mla_topk_select(const smla_topk_dims* dims, const float* scores, const int32_t* seq_lens,
                            int32_t* topk_idx, uint32_t* err_word, smla_stream_t stream);
 
 /* The launch shape sparse_mla_topk_select uses for dims on a device with
- * sm_count SMs (host only, no CUDA call): *cluster_ctas CTAs per query row,
- * each holding *chunk_positions positions (a multiple of 512, at most 49152,
- * cluster_ctas x chunk_positions >= num_cols).  dims->cluster_ctas > 0 is
- * kept as given.  Returns SMLA_ERR_INVALID_ARG for bad shapes or pointers,
+ * sm_count SMs (host only, no CUDA call): clusters of *cluster_ctas CTAs,
+ * each CTA holding *chunk_positions positions of one row (a multiple of 2048,
+ * at most 65536, cluster_ctas x chunk_positions >= num_cols).  A row spans
+ * at most one cluster; with a power-of-two cluster size, rows that need fewer
+ * chunks than the cluster has CTAs share clusters (packed by their chunk
+ * count on the device, from seq_lens).  dims->cluster_ctas > 0 is kept as
+ * given.  Returns SMLA_ERR_INVALID_ARG for bad shapes or pointers,
  * SMLA_ERR_UNSUPPORTED when no shape fits. */
 int sparse_mla_topk_plan_for(const smla_topk_dims* dims, int32_t sm_count, int32_t* cluster_ctas,
                              int32_t* chunk_positions);

@@ -66,10 +66,11 @@ struct AppendParams {
   uint32_t* err;              // device error word (may be null)
 };
 
-// Top-k selection (one cluster of csize CTAs per query row, chunk positions per CTA).
+// Top-k selection (clusters of csize CTAs, chunk positions per CTA; a row spans at most one cluster).
 constexpr int kTopkPortableCluster = 8;  // cluster sizes every launch supports
 constexpr int kTopkMaxCluster = 16;      // with the non-portable cluster size attribute (rows past 8 chunks)
-constexpr int kTopkMaxChunk = 49152;   // scores per CTA (192 KB of keys in shared memory)
+constexpr int kTopkMaxChunk = 65536;     // scores per CTA (chunk indexes are 16-bit)
+constexpr int kTopkChunkAlign = 2048;    // chunks are multiples of this (16 warps x 128-entry steps)
 struct TopkParams {
   const float* scores;        // [batch][stride]
   const int32_t* seq_lens;    // [batch]
@@ -78,6 +79,8 @@ struct TopkParams {
   int64_t stride;
   int num_cols, k, chunk, csize;
   int vec4;                   // scores 16-byte aligned and stride % 4 == 0: 16-byte loads
+  int batch;                  // rows (set by launch_topk)
+  int pack;                   // csize a power of two > 1: rows packed into clusters by their chunk count
 };
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk);
 size_t topk_smem_bytes(int chunk);

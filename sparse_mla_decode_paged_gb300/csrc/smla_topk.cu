@@ -5,23 +5,31 @@
 // position, and write them in increasing position order; when len_b <= k keep every position and
 // pad with -1.
 //
-// One thread-block cluster per query row.  The row is cut into csize contiguous chunks, one per CTA
-// of the cluster, loaded once from HBM (16-byte streaming loads) into shared memory as 32-bit order
-// keys.  Selection is a radix select in two stages; every decision is taken identically by every CTA
-// of the cluster from sums that each CTA pushes into all the others' shared memory (remote reductions)
-// before a cluster barrier, so after the barrier each CTA reads only its own shared memory, no CTA
-// leads and nothing waits on a flag:
-//   1. a coarse 8-bit bin that is monotone in the key (sign, exponent within a 32-octave window, two
-//      mantissa bits), histogrammed while the chunk loads (per-warp histograms): bins above the one
-//      holding the k-th key are kept whole, bins below are dropped;
-//   2. the entries of that bin (the candidates, listed per warp) are refined digit by digit, starting
-//      below the leading bits all candidates share (from the cluster's smallest and largest
-//      candidate); the select stops as soon as a digit's bin is kept whole.
-// The outcome is one threshold key; an order-preserving compaction (per-warp ballots, per-warp and
-// per-CTA bases) writes the kept positions in position order.
+// A row is cut into chunks of `chunk` positions, one per CTA; the CTAs of a row sit in one
+// thread-block cluster.  With a power-of-two cluster size the rows are packed: a row of u chunks takes
+// an aligned group of u' CTAs (u' = u rounded up to a power of two), the groups ordered by size, so a
+// cluster holds one long row or several short ones and a ragged batch does not give every row a whole
+// cluster.  Nothing per position stays in shared memory (so two CTAs fit on an SM whatever the chunk):
+// each warp streams its contiguous segment of the chunk twice, once from HBM (16-byte streaming loads)
+// and once more from L2, as 32-bit order keys.  Selection is a radix select in 11-, 11- and 10-bit
+// digits: every decision is taken identically by every CTA of the row from digit histograms that each
+// CTA adds into all the row's CTAs' shared memory (remote reductions) before a cluster barrier, so
+// after the barrier each CTA reads only its own shared memory, no CTA leads and nothing waits on a
+// flag:
+//   1. the top digit (sign, exponent, two mantissa bits), histogrammed on the first pass: digits above
+//      the one holding the k-th key are kept whole, digits below dropped;
+//   2. the second pass lists, per warp and in position order, the entries at or above that digit (the
+//      kept-for-sure entries and the candidates) with their keys;
+//   3. the candidates are refined digit by digit from the lists; the select stops as soon as a
+//      digit's bin is kept whole.
+// The outcome is one threshold key; per-warp counts over the lists, the counts of the row's lower CTAs
+// (one more exchange) and ballots over the lists write the kept positions in position order.  A warp
+// whose entries overflow its list reads its segment again from global memory at each of those steps.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
+#include <cstddef>
 #include <mutex>
 
 #include "smla_internal.h"
@@ -34,30 +42,32 @@ using namespace ptx;
 
 constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kTkBins = 256;
-constexpr int kTkRefinePasses = 4;   // at most 32 bits in 8-bit digits
-constexpr int kTkLoadUnroll = 4;     // 16-byte loads in flight per thread
-constexpr int kTkWarpCands = 512;    // candidate indexes listed per warp (16-bit, in the histogram space)
-constexpr int kTkWindowLo = 111;     // biased exponent of the coarse window's lowest octave (2^-16)
+constexpr int kTkBins = 2048;          // 11-bit digits: key bits 31..21, then 20..10
+constexpr int kTkLastBins = 1024;      // the last digit: key bits 9..0
+constexpr int kTkLoadUnroll = 4;       // 16-byte (or 4-byte) loads in flight per thread
+constexpr int kTkWarpList = 512;       // entries listed per warp
+constexpr int kTkMaxClass = 4;         // packed row groups of 1, 2, 4, 8 or 16 CTAs
+constexpr int kTkRowsCached = 4;       // row lengths a thread keeps while the rows are packed
+// launch-shape model of topk_plan: us per wave, per chunk position (per CTA sharing the SM), per cluster
+constexpr double kTkFixedUs = 4.0, kTkPosUs = 0.25e-3, kTkClusterUs = 3.0;
 
 struct TkShared {
+  // row-wide digit histograms, accumulated by remote reductions from every CTA of the row: the top
+  // digit in [0], the second in [1], the last in [0] again (cleared once the top digit is picked)
+  uint32_t hsum[2][kTkBins];
   union {
-    uint32_t whist[kTkWarps][kTkBins];       // per-warp coarse histograms while the chunk loads
-    uint16_t cand[kTkWarps][kTkWarpCands];   // then: chunk indexes of each warp's candidates
+    uint32_t hloc[kTkBins];                  // this CTA's top-digit histogram while the chunk loads
+    struct {                                 // then per warp, in position order:
+      uint32_t key[kTkWarps][kTkWarpList];   //   the full order keys of the listed entries
+      uint16_t idx[kTkWarps][kTkWarpList];   //   and their chunk indexes
+    } l;
   } u;
-  // cluster-wide sums, accumulated by remote reductions from every CTA of the cluster
-  uint32_t hist_c[kTkBins];                  // coarse histogram
-  uint32_t hist[kTkRefinePasses][kTkBins];   // refinement histograms
-  // this CTA's own refinement histograms (pushed into the sums above)
-  uint32_t hloc[kTkRefinePasses][kTkBins];
-  uint32_t cmin, cmax;                       // smallest and largest candidate key
-  uint32_t peer_cnt[kTopkMaxCluster][2];     // per CTA: kept-for-sure entries, tie-class entries
-  // this CTA only
-  uint32_t wcand[kTkWarps];                  // candidates per warp
-  uint32_t wcnt[2][kTkWarps];                // per warp: kept-for-sure entries, tie-class entries
+  uint32_t wgt[kTkWarps], weq[kTkWarps];     // per warp: kept-for-sure entries, tie-class entries
   uint32_t wbase[2][kTkWarps];               // per warp: output base, tie-rank base
   uint32_t scan[kTkWarps];
-  uint32_t overflow;                         // a warp listed more candidates than it holds
+  uint32_t peer_cnt[kTopkMaxCluster][2];     // per lower CTA of the row: kept-for-sure, tie-class entries
+  uint32_t ncls[kTkMaxClass + 1];            // rows per packed group size
+  int row_found, row_len;
   uint32_t bc, need, done;
 };
 
@@ -67,79 +77,45 @@ __device__ __forceinline__ uint32_t order_key(uint32_t bits) {
   return (bits & 0x80000000u) ? ~bits : (bits | 0x80000000u);
 }
 
-// Coarse bin of a key, monotone (non-decreasing) in the key: 128 + idx for a positive value, 127 - idx
-// for a negative one, idx = 4 (exponent - 111) + top two mantissa bits clamped to [0, 127] (magnitudes
-// below 2^-16 share idx 0, those from 2^16 up, with the infinities and NaNs, share idx 127).
-__device__ __forceinline__ uint32_t coarse_bin(uint32_t key) {
-  const bool pos = (key >> 31) != 0;
-  const uint32_t mag = (pos ? key : ~key) & 0x7FFFFFFFu;
-  int idx = (int)(mag >> 21) - 4 * kTkWindowLo;
-  idx = idx < 0 ? 0 : idx > 127 ? 127 : idx;
-  return pos ? 128u + (uint32_t)idx : 127u - (uint32_t)idx;
-}
-
-// Smallest key whose coarse bin is bc (coarse_bin is monotone, so bin bc is the key interval
-// [coarse_lo(bc), coarse_lo(bc + 1) - 1]).
-__device__ __forceinline__ uint32_t coarse_lo(uint32_t bc) {
-  if (bc >= 128u) {  // positive values: the smallest magnitude of index bc - 128
-    const uint32_t idx = bc - 128u;
-    return idx == 0 ? 0x80000000u : (0x80000000u | ((idx + 4u * kTkWindowLo) << 21));
-  }
-  const uint32_t idx = 127u - bc;  // negative values: the largest magnitude of index 127 - bc
-  if (idx == 127u) return 0u;
-  const uint32_t mag = ((idx + 4u * kTkWindowLo + 1u) << 21) - 1u;
-  return ~(0x80000000u | mag);
-}
-
-__device__ __forceinline__ uint32_t coarse_hi(uint32_t bc) { return bc == 255u ? 0xFFFFFFFFu : coarse_lo(bc + 1u) - 1u; }
-
-// Remote reductions into the shared memory of CTA `rank` of the cluster (any CTA, this one included).
+// Remote reductions and stores into the shared memory of CTA `rank` of the cluster (this one included).
 __device__ __forceinline__ void red_add_cluster(uint32_t saddr, uint32_t rank, uint32_t v) {
   asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(mapa(saddr, rank)), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_min_cluster(uint32_t saddr, uint32_t rank, uint32_t v) {
-  asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(mapa(saddr, rank)), "r"(v) : "memory");
-}
-__device__ __forceinline__ void red_max_cluster(uint32_t saddr, uint32_t rank, uint32_t v) {
-  asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(mapa(saddr, rank)), "r"(v) : "memory");
 }
 __device__ __forceinline__ void st_cluster_u32(uint32_t saddr, uint32_t rank, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(mapa(saddr, rank)), "r"(v) : "memory");
 }
 
+// Every thread of the cluster, or of this CTA when the launch has no cluster.
+__device__ __forceinline__ void row_sync(int csize) {
+  if (csize > 1) cluster_sync_all();
+  else __syncthreads();
+}
 
-// Adds the active lanes' bins to histogram h (this CTA's shared memory); the lanes sharing the first
-// active lane's bin add with one atomic (a tie-heavy row puts whole warps in one bin).  Every lane of
-// the warp calls it.
-__device__ __forceinline__ void hist_add(uint32_t* h, bool active, uint32_t bin) {
+// The row group a CTA works in: `gsz` CTAs of cluster ranks g0 .. g0 + gsz - 1, this CTA the sub-th.
+struct TkGroup {
+  int g0, gsz;
+  // Adds v to bin `bin` of the histogram h in every CTA of the group.
+  __device__ __forceinline__ void add(uint32_t* h, uint32_t bin, uint32_t v) const {
+    if (gsz == 1) {
+      atomicAdd(h + bin, v);
+    } else {
+      const uint32_t a = smem_u32(h + bin);
+      for (int r = 0; r < gsz; ++r) red_add_cluster(a, (uint32_t)(g0 + r), v);
+    }
+  }
+};
+
+// Adds the active lanes' bins to histogram h of every CTA of the group; the lanes sharing the first
+// active lane's bin add with one reduction (a tie-heavy row puts whole warps in one bin).  Every lane
+// of the warp calls it.
+__device__ __forceinline__ void hist_add(const TkGroup& grp, uint32_t* h, bool active, uint32_t bin) {
   const unsigned act = __ballot_sync(0xffffffffu, active);
   if (!act) return;
   const int leader = __ffs(act) - 1;
   const uint32_t lb = __shfl_sync(0xffffffffu, bin, leader);
   const unsigned same = __ballot_sync(0xffffffffu, active && bin == lb);
-  if ((int)(threadIdx.x & 31) == leader) atomicAdd(h + lb, (uint32_t)__popc(same));
-  else if (active && bin != lb) atomicAdd(h + bin, 1u);
-}
-
-// Every thread of the row's CTAs (the cluster), or of this CTA when the row has one.
-__device__ __forceinline__ void row_barrier(int csize) {
-  if (csize > 1) cluster_sync_all();
-  else __syncthreads();
-}
-
-// Adds this CTA's 256-bin histogram `local` into the cluster-wide sum `sum` of every CTA of the
-// cluster (thread t < 256 pushes bin t).
-__device__ __forceinline__ void push_hist(const uint32_t* local, uint32_t* sum, int csize) {
-  const int t = threadIdx.x;
-  if (t < kTkBins) {
-    const uint32_t v = local[t];
-    if (csize == 1) {
-      sum[t] += v;
-    } else if (v != 0) {
-      const uint32_t a = smem_u32(sum + t);
-      for (int r = 0; r < csize; ++r) red_add_cluster(a, (uint32_t)r, v);
-    }
-  }
+  if ((int)(threadIdx.x & 31) == leader) grp.add(h, lb, (uint32_t)__popc(same));
+  else if (active && bin != lb) grp.add(h, bin, 1u);
 }
 
 // Kept entries of the tie class among `e` entries, given `before` such entries at lower positions.
@@ -148,34 +124,51 @@ __device__ __forceinline__ uint32_t kept_ties(uint32_t before, uint32_t e, uint3
   return min(need - before, e);
 }
 
-// Finds in the cluster-wide histogram h the bin holding the need-th largest entry.  Threads 0..255
-// take bins 255..0, so an inclusive scan in thread order sums the bins from the top.  The one thread
-// whose bin it is writes s.bc (the bin), s.need (the rank within it) and s.done (the bin is kept
-// whole).  All threads call it; it ends with a block barrier.
+// Finds in the row-wide histogram h (NB bins) the bin holding the need-th largest entry.  Thread t
+// takes bins NB - 1 - BPT t - i (i < BPT), so an inclusive scan in thread order sums the bins from the
+// top.  The one thread whose bin it is writes s.bc (the bin), s.need (the rank within it) and s.done
+// (the bin is kept whole).  All threads of the CTA call it; it ends with a block barrier.
+template <int NB>
 __device__ __forceinline__ void pick_bin(TkShared& s, const uint32_t* h, uint32_t need) {
+  constexpr int BPT = NB / kTkThreads;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint32_t g = 0, incl = 0;
-  if (tid < kTkBins) {
-    g = h[kTkBins - 1 - tid];
-    incl = g;
+  uint32_t g[BPT], sum = 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+  for (int i = 0; i < BPT; ++i) {
+    g[i] = h[NB - 1 - BPT * tid - i];
+    sum += g[i];
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s.scan[warp] = incl;
+  __syncthreads();
+  for (int w = 0; w < warp; ++w) incl += s.scan[w];
+  uint32_t run = incl - sum;
+  if (run < need && need <= incl) {
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+      if (run < need && need <= run + g[i]) {
+        s.bc = (uint32_t)(NB - 1 - BPT * tid - i);
+        s.need = need - run;
+        s.done = (g[i] == need - run) ? 1u : 0u;
+      }
+      run += g[i];
     }
-    if (lane == 31) s.scan[warp] = incl;
   }
   __syncthreads();
-  if (tid < kTkBins) {
-    for (int w = 0; w < warp; ++w) incl += s.scan[w];
-    const uint32_t excl = incl - g;
-    if (excl < need && need <= incl) {
-      s.bc = (uint32_t)(kTkBins - 1 - tid);
-      s.need = need - excl;
-      s.done = (g == need - excl) ? 1u : 0u;
-    }
+}
+
+// Adds this CTA's histogram `local` into the row-wide sum `sum` of every CTA of the group.
+__device__ __forceinline__ void push_hist(const TkGroup& grp, const uint32_t* local, uint32_t* sum) {
+  for (int bin = threadIdx.x; bin < kTkBins; bin += kTkThreads) {
+    const uint32_t v = local[bin];
+    if (grp.gsz == 1) sum[bin] = v;
+    else if (v != 0) grp.add(sum, (uint32_t)bin, v);
   }
-  __syncthreads();
 }
 
 // The final rule: an entry is kept for sure when all_kept or key > t, and is in the tie class (kept in
@@ -187,209 +180,338 @@ struct TkRule {
   __device__ __forceinline__ bool eq(uint32_t key) const { return ties && key == t; }
 };
 
+// Length of row b clamped to [0, num_cols], and its packed group size class: log2 of the chunks it
+// spans rounded up to a power of two (a row of at most one chunk, or none, has class 0).
+__device__ __forceinline__ int clamp_len(const TopkParams& p, int len) {
+  return len < 0 ? 0 : len > p.num_cols ? p.num_cols : len;
+}
+__device__ __forceinline__ int len_class(const TopkParams& p, int len) {
+  const int u = (clamp_len(p, len) + p.chunk - 1) / p.chunk;
+  return u <= 1 ? 0 : 32 - __clz(u - 1);
+}
+
+// Order key of score i of a row (a reread: L2 holds the rows just loaded).
+__device__ __forceinline__ uint32_t key_at(const float* row, int i) {
+  return order_key(__ldg(reinterpret_cast<const unsigned int*>(row) + i));
+}
+
 __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
-  extern __shared__ __align__(16) uint32_t keys[];
-  TkShared& s = *reinterpret_cast<TkShared*>(keys + p.chunk);
-  const int csize = p.csize;
-  const int rank = csize > 1 ? (int)cluster_ctarank() : 0;
-  const int b = blockIdx.x / csize;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TkShared& s = *reinterpret_cast<TkShared*>(smem_raw);
+  const int cs = p.csize;
+  const int rank = cs > 1 ? (int)cluster_ctarank() : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned below = (1u << lane) - 1u;
 
-  int len = __ldg(p.seq_lens + b);
-  if (len < 0 || len > p.num_cols) {
-    if (rank == 0 && tid == 0 && p.err) atomicOr(p.err, SMLA_DEVERR_LEN_RANGE);
-    len = len < 0 ? 0 : p.num_cols;
-  }
-  const int c0 = rank * p.chunk;
-  const int n = max(0, min(len - c0, p.chunk));
-  int32_t* out = p.out + (size_t)b * p.k;
-
-  // a short row keeps every position (the same branch in every CTA of the cluster)
-  if (len <= p.k) {
-    for (int i = tid; i < n; i += kTkThreads) out[c0 + i] = c0 + i;
-    if (rank == 0)
-      for (int i = len + tid; i < p.k; i += kTkThreads) out[i] = -1;
-    return;
-  }
-
-  for (int i = tid; i < kTkWarps * kTkBins; i += kTkThreads) (&s.u.whist[0][0])[i] = 0;
-  for (int i = tid; i < kTkBins; i += kTkThreads) s.hist_c[i] = 0;
-  for (int i = tid; i < kTkRefinePasses * kTkBins; i += kTkThreads) {
-    (&s.hist[0][0])[i] = 0;
-    (&s.hloc[0][0])[i] = 0;
-  }
-  if (tid < 2 * kTopkMaxCluster) (&s.peer_cnt[0][0])[tid] = 0;
-  if (tid == 0) {
-    s.cmin = 0xFFFFFFFFu;
-    s.cmax = 0;
-    s.overflow = 0;
-  }
-  // the cluster's sums are zero everywhere before any CTA pushes into them; the barrier completes
-  // while the chunk loads
-  if (csize > 1) cluster_arrive_release();
-  __syncthreads();
-
-  // load the chunk as order keys, with the coarse histogram
-  uint32_t* wh = s.u.whist[warp];
-  const float* row = p.scores + (size_t)b * p.stride + c0;
-  if (p.vec4) {
-    const int n4 = n >> 2;
-    for (int base = 0; base < n4; base += kTkThreads * kTkLoadUnroll) {
-      uint4 v[kTkLoadUnroll];
-#pragma unroll
-      for (int u = 0; u < kTkLoadUnroll; ++u) {
-        const int j = base + u * kTkThreads + tid;
-        if (j < n4) v[u] = ldg_stream(row + 4 * j);
-      }
-#pragma unroll
-      for (int u = 0; u < kTkLoadUnroll; ++u) {
-        const int j = base + u * kTkThreads + tid;
-        if (j < n4) {
-          const uint4 kk = make_uint4(order_key(v[u].x), order_key(v[u].y), order_key(v[u].z), order_key(v[u].w));
-          reinterpret_cast<uint4*>(keys)[j] = kk;
-          atomicAdd(wh + coarse_bin(kk.x), 1u);
-          atomicAdd(wh + coarse_bin(kk.y), 1u);
-          atomicAdd(wh + coarse_bin(kk.z), 1u);
-          atomicAdd(wh + coarse_bin(kk.w), 1u);
-        }
-      }
-    }
-    const int i = (n4 << 2) + tid;  // at most three scalar tail entries
-    if (tid < (n & 3)) {
-      const uint32_t kk = order_key(__float_as_uint(__ldg(row + i)));
-      keys[i] = kk;
-      atomicAdd(wh + coarse_bin(kk), 1u);
-    }
+  // ---- the row of this CTA, its place in the row, and the row's CTAs (its group)
+  int row = -1, sub = 0, raw_len = 0;
+  TkGroup grp{rank, 1};
+  if (!p.pack) {
+    row = (int)blockIdx.x / cs;
+    sub = rank;
+    grp = TkGroup{0, cs};
+    raw_len = __ldg(p.seq_lens + row);
   } else {
-    for (int base = 0; base < n; base += kTkThreads * kTkLoadUnroll) {
-      uint32_t v[kTkLoadUnroll];
+    // groups in decreasing size, rows in index order within a size: group starts are multiples of
+    // their size, so no group crosses a cluster.  Every CTA reads all lengths once (the first
+    // kTkRowsCached per thread stay in registers for the search below).
+    const int top = 31 - __clz(cs);
+    if (tid <= kTkMaxClass) s.ncls[tid] = 0;
+    if (tid == 0) s.row_found = -1;
+    int lens_c[kTkRowsCached];
 #pragma unroll
-      for (int u = 0; u < kTkLoadUnroll; ++u) {
-        const int i = base + u * kTkThreads + tid;
-        if (i < n) v[u] = __float_as_uint(__ldg(row + i));
-      }
+    for (int i = 0; i < kTkRowsCached; ++i) {
+      const int b = i * kTkThreads + tid;
+      lens_c[i] = b < p.batch ? __ldg(p.seq_lens + b) : 0;
+    }
+    // length of row b = i * kTkThreads + tid (this thread's i-th row)
+    auto len_of = [&](int i, int b) {
+      int v = 0;
 #pragma unroll
-      for (int u = 0; u < kTkLoadUnroll; ++u) {
-        const int i = base + u * kTkThreads + tid;
-        if (i < n) {
-          const uint32_t kk = order_key(v[u]);
-          keys[i] = kk;
-          atomicAdd(wh + coarse_bin(kk), 1u);
-        }
+      for (int r = 0; r < kTkRowsCached; ++r)
+        if (r == i) v = lens_c[r];
+      return i < kTkRowsCached ? v : (b < p.batch ? __ldg(p.seq_lens + b) : 0);
+    };
+    __syncthreads();
+    for (int b0 = 0, i = 0; b0 < p.batch; b0 += kTkThreads, ++i) {
+      const int b = b0 + tid;
+      const int len_b = len_of(i, b);
+      const int c = b < p.batch ? len_class(p, len_b) : -1;
+      for (int j = 0; j <= top; ++j) {
+        const unsigned m = __ballot_sync(0xffffffffu, c == j);
+        if (lane == 0 && m) atomicAdd(&s.ncls[j], (uint32_t)__popc(m));
       }
     }
+    __syncthreads();
+    const uint32_t g = blockIdx.x;
+    uint32_t off = 0, my_off = 0;
+    int my_cls = -1;
+    for (int j = top; j >= 0; --j) {
+      const uint32_t span = s.ncls[j] << j;
+      if (my_cls < 0 && g < off + span) {
+        my_cls = j;
+        my_off = off;
+      }
+      off += span;
+    }
+    if (g - (uint32_t)rank >= off) return;  // the whole cluster lies past the packed rows
+    if (my_cls >= 0) {
+      grp.gsz = 1 << my_cls;
+      sub = (int)((g - my_off) & (uint32_t)(grp.gsz - 1));
+      grp.g0 = rank - sub;
+      const uint32_t q = (g - my_off) >> my_cls;  // rank of the row among the rows of its class
+      uint32_t seen = 0;
+      for (int b0 = 0, i = 0; b0 < p.batch; b0 += kTkThreads, ++i) {  // block-uniform trip count
+        const int b = b0 + tid;
+        const int len_b = len_of(i, b);
+        const bool is = b < p.batch && len_class(p, len_b) == my_cls;
+        const unsigned m = __ballot_sync(0xffffffffu, is);
+        if (lane == 0) s.scan[warp] = (uint32_t)__popc(m);
+        __syncthreads();
+        uint32_t before = seen;
+        for (int w = 0; w < kTkWarps; ++w) {
+          if (w < warp) before += s.scan[w];
+          seen += s.scan[w];
+        }
+        if (is && before + (uint32_t)__popc(m & below) == q) {
+          s.row_found = b;
+          s.row_len = len_b;
+        }
+        __syncthreads();
+        if (s.row_found >= 0) break;
+      }
+      row = s.row_found;
+      raw_len = s.row_len;
+    }
   }
+
+  int len = 0;
+  if (row >= 0) {
+    len = clamp_len(p, raw_len);
+    if (len != raw_len && sub == 0 && tid == 0 && p.err) atomicOr(p.err, SMLA_DEVERR_LEN_RANGE);
+  }
+  const int c0 = sub * p.chunk;
+  const int n = row >= 0 ? max(0, min(len - c0, p.chunk)) : 0;
+  int32_t* out = p.out + (size_t)(row >= 0 ? row : 0) * p.k;
+  const float* row_src = p.scores + (size_t)(row >= 0 ? row : 0) * p.stride;
+  const bool active = row >= 0 && len > p.k;
+
+  // a short row keeps every position
+  if (row >= 0 && !active) {
+    for (int i = tid; i < n; i += kTkThreads) out[c0 + i] = c0 + i;
+    if (sub == 0)
+      for (int i = len + tid; i < p.k; i += kTkThreads) out[i] = -1;
+  }
+  // a cluster holding one row takes every decision below uniformly; one that holds several rows (or
+  // idle CTAs) runs every exchange, each row skipping the work it does not need
+  const bool uniform = grp.gsz == cs && row >= 0;
+  if (uniform && !active) return;
+
+  // the row-wide sums are zero everywhere before any CTA pushes into them; the barrier completes while
+  // the chunk loads
+  if (active) {
+    uint4* z = reinterpret_cast<uint4*>(&s.hsum[0][0]);
+    constexpr int kZero = (2 * kTkBins + kTkBins) / 4;  // hsum and hloc
+    static_assert(offsetof(TkShared, u) == offsetof(TkShared, hsum) + sizeof(uint32_t) * 2 * kTkBins,
+                  "hloc follows hsum");
+    for (int i = tid; i < kZero; i += kTkThreads) z[i] = make_uint4(0, 0, 0, 0);
+  }
+  if (cs > 1) cluster_arrive_release();
   __syncthreads();
-  if (tid < kTkBins) {
-    uint32_t t = 0;
-#pragma unroll
-    for (int w = 0; w < kTkWarps; ++w) t += s.u.whist[w][tid];
-    s.u.whist[0][tid] = t;  // this CTA's coarse histogram
-  }
-  if (csize > 1) cluster_wait();  // every CTA's sums are zeroed
-  push_hist(s.u.whist[0], s.hist_c, csize);
-  row_barrier(csize);  // the coarse sums are complete
 
-  pick_bin(s, s.hist_c, (uint32_t)p.k);
-  const uint32_t bc = s.bc;
-  const uint32_t clo = coarse_lo(bc), chi = coarse_hi(bc);
-  uint32_t need = s.need, prefix = 0;
-  bool done = s.done != 0;
-
-  if (!done) {
-    // each warp lists its candidates (coarse bin bc: keys in [clo, chi]) from its contiguous segment;
-    // the per-warp histograms are dead (summed above), so their space holds the lists
-    const int seg = p.chunk / kTkWarps;
-    const int s0 = warp * seg;
-    const int s_end = min(seg, n - s0);  // warp-uniform; may be <= 0
-    uint16_t* my = s.u.cand[warp];
-    uint32_t cnt = 0, lo = 0xFFFFFFFFu, hi = 0;
-    const unsigned below = (1u << lane) - 1u;
-    for (int j0 = 0; j0 < s_end; j0 += 128) {  // warp-uniform; entries j0 + 32 q + lane, q = 0..3
-      uint32_t kq[4];
+  // ---- first pass over the warp's segment of the chunk (HBM): the top-digit histogram
+  // the CTA's n positions in 16 contiguous segments of whole 128-entry steps (a short chunk spreads
+  // over every warp, so that no warp lists more than its share)
+  const int seg = ((n + kTkWarps - 1) / kTkWarps + 127) & ~127;
+  const int s0 = warp * seg;
+  const int s_len = max(0, min(seg, n - s0));  // warp-uniform
+  const float* src = row_src + c0 + s0;         // this warp's segment
+  if (active) {
+    uint32_t* h = s.u.hloc;
+    if (p.vec4) {
+      const int n4 = s_len >> 2;
+      for (int base = 0; base < n4; base += 32 * kTkLoadUnroll) {
+        uint4 v[kTkLoadUnroll];
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + 32 * q + lane;
-        kq[q] = j < s_end ? keys[s0 + j] : 0u;
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = j0 + 32 * q + lane;
-        const bool c = j < s_end && kq[q] >= clo && kq[q] <= chi;
-        const unsigned cb = __ballot_sync(0xffffffffu, c);
-        if (c) {
-          const uint32_t at = cnt + (uint32_t)__popc(cb & below);
-          if (at < (uint32_t)kTkWarpCands) my[at] = (uint16_t)(s0 + j);
-          lo = min(lo, kq[q]);
-          hi = max(hi, kq[q]);
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int j = base + 32 * u + lane;
+          if (j < n4) v[u] = ldg_stream(src + 4 * j);
         }
-        cnt += (uint32_t)__popc(cb);
-      }
-    }
-    lo = __reduce_min_sync(0xffffffffu, lo);
-    hi = __reduce_max_sync(0xffffffffu, hi);
-    if (lane == 0) {
-      s.wcand[warp] = cnt;
-      if (cnt > (uint32_t)kTkWarpCands) s.overflow = 1;
-      if (cnt) {
-        if (csize == 1) {
-          atomicMin(&s.cmin, lo);
-          atomicMax(&s.cmax, hi);
-        } else {
-          for (int r = 0; r < csize; ++r) {
-            red_min_cluster(smem_u32(&s.cmin), (uint32_t)r, lo);
-            red_max_cluster(smem_u32(&s.cmax), (uint32_t)r, hi);
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int j = base + 32 * u + lane;
+          if (j < n4) {
+            atomicAdd(h + (order_key(v[u].x) >> 21), 1u);
+            atomicAdd(h + (order_key(v[u].y) >> 21), 1u);
+            atomicAdd(h + (order_key(v[u].z) >> 21), 1u);
+            atomicAdd(h + (order_key(v[u].w) >> 21), 1u);
           }
         }
       }
+      if (lane < (s_len & 3)) atomicAdd(h + (key_at(src, (n4 << 2) + lane) >> 21), 1u);  // scalar tail
+    } else {
+      for (int base = 0; base < s_len; base += 32 * kTkLoadUnroll) {
+        uint32_t v[kTkLoadUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int i = base + 32 * u + lane;
+          if (i < s_len) v[u] = __ldg(reinterpret_cast<const unsigned int*>(src) + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u)
+          if (base + 32 * u + lane < s_len) atomicAdd(h + (order_key(v[u]) >> 21), 1u);
+      }
     }
-    row_barrier(csize);  // the candidate key range is complete
+  }
+  __syncthreads();
+  if (cs > 1) cluster_wait();  // every CTA's sums are zeroed
+  if (active) push_hist(grp, s.u.hloc, s.hsum[0]);
+  row_sync(cs);  // the row's top-digit sums are complete (and hloc is read: the lists take its space)
 
-    // every candidate shares the leading bits common to the smallest and largest one
-    const uint32_t gmin = s.cmin, gmax = s.cmax;
-    const int common = __clz(gmin ^ gmax);  // 32 when they are equal
-    uint32_t mask = common == 0 ? 0u : common == 32 ? 0xFFFFFFFFu : (0xFFFFFFFFu << (32 - common));
-    prefix = gmin & mask;
-    const bool listed = s.overflow == 0;
-    const uint32_t my_cnt = s.wcand[warp];
-    int rest = 32 - common;
-    for (int pass = 0; rest > 0 && !done; ++pass) {
-      const int w = rest < 8 ? rest : 8;
-      const int shift = rest - w;
-      const uint32_t dmask = (1u << w) - 1u;
-      uint32_t* hloc = s.hloc[pass];
+  uint32_t need = (uint32_t)p.k, prefix = 0, mask = 0;
+  bool done = false;
+  if (active) {
+    pick_bin<kTkBins>(s, s.hsum[0], need);
+    prefix = s.bc << 21;
+    mask = 0xFFE00000u;
+    need = s.need;
+    done = s.done != 0;
+    // clear the top-digit sums for the last digit (before the next cluster barrier)
+    for (int i = tid; i < kTkBins / 4; i += kTkThreads)
+      reinterpret_cast<uint4*>(s.hsum[0])[i] = make_uint4(0, 0, 0, 0);
+  }
+
+  // ---- second pass (L2): list this warp's entries >= prefix in position order, with their keys
+  uint32_t my_cnt = 0;  // entries of this warp at or above prefix (the list holds the first kTkWarpList)
+  uint32_t* lk = s.u.l.key[warp];
+  uint16_t* li = s.u.l.idx[warp];
+  // appends this lane's entries e0 + i (raw score bits x[i]) whose hit[i] is set, after those of the
+  // lower lanes (a run of consecutive positions, four a lane, lane-major); every lane calls it
+  auto append4 = [&](const uint32_t (&x)[4], const bool (&hit)[4], int e0) {
+    if (!__any_sync(0xffffffffu, hit[0] || hit[1] || hit[2] || hit[3])) return;
+    unsigned m[4];
+    uint32_t at = my_cnt, total = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      m[i] = __ballot_sync(0xffffffffu, hit[i]);
+      at += (uint32_t)__popc(m[i] & below);
+      total += (uint32_t)__popc(m[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (hit[i]) {
+        if (at < (uint32_t)kTkWarpList) {
+          lk[at] = order_key(x[i]);
+          li[at] = (uint16_t)(e0 + i);
+        }
+        ++at;
+      }
+    my_cnt += total;
+  };
+  if (active) {
+    // order_key(x) >= prefix as one compare on the raw bits x: with prefix in the positive half, x read
+    // as a signed integer reaches prefix's magnitude bits; otherwise x (unsigned) is at most ~prefix
+    const bool pos_lo = (prefix >> 31) != 0;
+    const int lo_s = (int)(prefix & 0x7FFFFFFFu);
+    const uint32_t lo_u = ~prefix;
+    auto reach = [&](uint32_t x) { return pos_lo ? (int)x >= lo_s : x <= lo_u; };
+    if (p.vec4) {
+      const int n4 = s_len >> 2;
+      for (int base = 0; base < n4; base += 32 * kTkLoadUnroll) {  // warp-uniform
+        uint4 v[kTkLoadUnroll];
+        bool ok[kTkLoadUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int j = base + 32 * u + lane;
+          ok[u] = j < n4;
+          if (ok[u]) v[u] = ldg_stream(src + 4 * j);
+        }
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int j = base + 32 * u + lane;
+          const uint32_t x[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+          const bool hit[4] = {ok[u] && reach(x[0]), ok[u] && reach(x[1]), ok[u] && reach(x[2]),
+                               ok[u] && reach(x[3])};
+          append4(x, hit, s0 + 4 * j);
+        }
+      }
+      // scalar tail: at most three entries, one a lane, after every quad
+      const int i = (n4 << 2) + lane;
+      const bool ok = lane < (s_len & 3);
+      const uint32_t xt = ok ? __ldg(reinterpret_cast<const unsigned int*>(src) + i) : 0u;
+      const uint32_t x[4] = {xt, 0u, 0u, 0u};
+      const bool hit[4] = {ok && reach(xt), false, false, false};
+      append4(x, hit, s0 + i);
+    } else {
+      for (int base = 0; base < s_len; base += 32 * kTkLoadUnroll) {  // warp-uniform
+        uint32_t v[kTkLoadUnroll];
+        bool okv[kTkLoadUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int i = base + 32 * u + lane;
+          okv[u] = i < s_len;
+          if (okv[u]) v[u] = __ldg(reinterpret_cast<const unsigned int*>(src) + i);
+        }
+#pragma unroll
+        for (int u = 0; u < kTkLoadUnroll; ++u) {
+          const int i = base + 32 * u + lane;
+          const uint32_t x[4] = {v[u], 0u, 0u, 0u};
+          const bool hit[4] = {okv[u] && reach(v[u]), false, false, false};
+          append4(x, hit, s0 + i);
+        }
+      }
+    }
+    __syncwarp();
+  }
+  const bool listed = my_cnt <= (uint32_t)kTkWarpList;
+  const uint32_t* lkey = lk;
+  const uint16_t* lidx = li;
+
+  // ---- refine the candidates: digit 2 (key bits 20..10) into hsum[1], digit 3 (bits 9..0) into hsum[0]
+#pragma unroll 1
+  for (int step = 0; step < 2; ++step) {
+    if (uniform && done) break;  // cluster-uniform (a single row decides identically everywhere)
+    const int shift = step == 0 ? 10 : 0;
+    const uint32_t dmask = step == 0 ? 0x7FFu : 0x3FFu;
+    uint32_t* h = s.hsum[step == 0 ? 1 : 0];
+    if (active && !done) {
       if (listed) {
         for (uint32_t c = lane; c < ((my_cnt + 31u) & ~31u); c += 32) {  // warp-uniform trip count
           const bool ok = c < my_cnt;
-          const uint32_t kk = ok ? keys[my[c]] : 0u;
-          hist_add(hloc, ok && (kk & mask) == prefix, (kk >> shift) & dmask);
+          const uint32_t kk = ok ? lkey[c] : 0u;
+          hist_add(grp, h, ok && (kk & mask) == prefix, (kk >> shift) & dmask);
         }
-      } else {  // a warp's list overflowed: every warp scans its segment for candidates
-        for (int j0 = 0; j0 < s_end; j0 += 32) {
-          const int j = j0 + lane;
-          const uint32_t kk = j < s_end ? keys[s0 + j] : 0u;
-          hist_add(hloc, j < s_end && kk >= clo && kk <= chi && (kk & mask) == prefix, (kk >> shift) & dmask);
+      } else {  // the list overflowed: read the segment again
+        for (int j0 = 0; j0 < s_len; j0 += 128) {
+          uint32_t kq[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int j = j0 + 32 * q + lane;
+            kq[q] = j < s_len ? key_at(src, j) : 0u;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            hist_add(grp, h, j0 + 32 * q + lane < s_len && (kq[q] & mask) == prefix, (kq[q] >> shift) & dmask);
         }
       }
-      __syncthreads();  // this CTA's digit histogram is complete
-      push_hist(hloc, s.hist[pass], csize);
-      row_barrier(csize);  // the digit sums are complete
-      pick_bin(s, s.hist[pass], need);
+    }
+    row_sync(cs);  // the digit sums are complete
+    if (active && !done) {
+      if (step == 0) pick_bin<kTkBins>(s, h, need);
+      else pick_bin<kTkLastBins>(s, h, need);
       prefix |= s.bc << shift;
       mask |= dmask << shift;
       need = s.need;
       done = s.done != 0;
-      rest -= w;
     }
   }
 
-  // done: the kept entries are exactly the keys >= max(prefix, clo) (the bins above bc whole, and the
-  // candidates from the prefix up); otherwise every bit is decided and prefix is the k-th key itself
+  // done: the kept entries are exactly the keys >= prefix (the bins above each chosen digit whole,
+  // and the last chosen bin whole); otherwise every bit is decided and prefix is the k-th key itself
   TkRule rule;
   if (done) {
-    const uint32_t lo = prefix > clo ? prefix : clo;
-    rule.all_kept = lo == 0;
-    rule.t = lo - 1u;
+    rule.all_kept = prefix == 0;
+    rule.t = prefix - 1u;
     rule.ties = false;
   } else {
     rule.all_kept = false;
@@ -397,48 +519,47 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
     rule.ties = true;
   }
 
-  // counts per warp segment (contiguous, a multiple of 32 entries): kept for sure, tie class
-  const int seg = p.chunk / kTkWarps;
-  const int s0 = warp * seg;
-  const int s_end = min(seg, n - s0);  // warp-uniform; may be <= 0
-  uint32_t c_gt = 0, c_eq = 0;
-  for (int j0 = 0; j0 < s_end; j0 += 128) {
-    uint32_t kq[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = j0 + 32 * q + lane;
-      kq[q] = j < s_end ? keys[s0 + j] : 0u;
+  // ---- per-warp counts: kept for sure, tie class
+  if (active) {
+    uint32_t c_gt = 0, c_eq = 0;
+    if (listed) {
+      for (uint32_t c = lane; c < my_cnt; c += 32) {
+        const uint32_t kk = lkey[c];
+        c_gt += rule.gt(kk);
+        c_eq += rule.eq(kk);
+      }
+    } else {
+      for (int j = lane; j < s_len; j += 32) {
+        const uint32_t kk = key_at(src, j);
+        c_gt += rule.gt(kk);
+        c_eq += rule.eq(kk);
+      }
     }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const bool ok = j0 + 32 * q + lane < s_end;
-      c_gt += ok && rule.gt(kq[q]);
-      c_eq += ok && rule.eq(kq[q]);
+    c_gt = __reduce_add_sync(0xffffffffu, c_gt);
+    c_eq = __reduce_add_sync(0xffffffffu, c_eq);
+    if (lane == 0) {
+      s.wgt[warp] = c_gt;
+      s.weq[warp] = c_eq;
     }
-  }
-  c_gt = __reduce_add_sync(0xffffffffu, c_gt);
-  c_eq = __reduce_add_sync(0xffffffffu, c_eq);
-  if (lane == 0) {
-    s.wcnt[0][warp] = c_gt;
-    s.wcnt[1][warp] = c_eq;
   }
   __syncthreads();
-  if (tid == 0) {
+  if (active && tid == 0 && grp.gsz > 1) {
     uint32_t a = 0, e = 0;
     for (int w = 0; w < kTkWarps; ++w) {
-      a += s.wcnt[0][w];
-      e += s.wcnt[1][w];
+      a += s.wgt[w];
+      e += s.weq[w];
     }
-    // CTAs of higher rank (later positions) need this CTA's counts
-    for (int r = rank + 1; r < csize; ++r) {
-      st_cluster_u32(smem_u32(&s.peer_cnt[rank][0]), (uint32_t)r, a);
-      st_cluster_u32(smem_u32(&s.peer_cnt[rank][1]), (uint32_t)r, e);
+    // the row's CTAs at later positions need this CTA's counts
+    for (int r = sub + 1; r < grp.gsz; ++r) {
+      st_cluster_u32(smem_u32(&s.peer_cnt[sub][0]), (uint32_t)(grp.g0 + r), a);
+      st_cluster_u32(smem_u32(&s.peer_cnt[sub][1]), (uint32_t)(grp.g0 + r), e);
     }
   }
-  if (csize > 1) cluster_sync_all();  // the counts of every lower-rank CTA are here (the last cluster-wide step)
+  if (cs > 1) cluster_sync_all();  // the counts of every lower CTA of the row are here (the last exchange)
+  if (!active) return;
   if (tid == 0) {
     uint32_t sel = 0, eq = 0;  // kept entries and tie entries at lower positions
-    for (int r = 0; r < rank; ++r) {
+    for (int r = 0; r < sub; ++r) {
       const uint32_t gt_r = s.peer_cnt[r][0], eq_r = s.peer_cnt[r][1];
       sel += gt_r + (rule.ties ? kept_ties(eq, eq_r, need) : 0u);
       eq += eq_r;
@@ -446,33 +567,34 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
     for (int w = 0; w < kTkWarps; ++w) {
       s.wbase[0][w] = sel;
       s.wbase[1][w] = eq;
-      sel += s.wcnt[0][w] + (rule.ties ? kept_ties(eq, s.wcnt[1][w], need) : 0u);
-      eq += s.wcnt[1][w];
+      sel += s.wgt[w] + (rule.ties ? kept_ties(eq, s.weq[w], need) : 0u);
+      eq += s.weq[w];
     }
   }
   __syncthreads();
 
-  // order-preserving write of this warp's kept positions
+  // ---- order-preserving write of this warp's kept positions
   uint32_t sel_base = s.wbase[0][warp], eq_base = s.wbase[1][warp];
-  const unsigned below = (1u << lane) - 1u;
-  for (int j0 = 0; j0 < s_end; j0 += 128) {  // warp-uniform; entries j0 + 32 q + lane, in position order
-    uint32_t kq[4];
+  const uint32_t trips = listed ? my_cnt : (uint32_t)s_len;
+  for (uint32_t c0w = 0; c0w < trips; c0w += 128) {  // warp-uniform; entries in position order
+    uint32_t kq[4], iq[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int j = j0 + 32 * q + lane;
-      kq[q] = j < s_end ? keys[s0 + j] : 0u;
+      const uint32_t c = c0w + 32 * q + lane;
+      const bool ok = c < trips;
+      iq[q] = ok ? (listed ? (uint32_t)lidx[c] : (uint32_t)s0 + c) : 0u;
+      kq[q] = ok ? (listed ? lkey[c] : key_at(row_src + c0, (int)iq[q])) : 0u;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const int j = j0 + 32 * q + lane;
-      const bool ok = j < s_end;
+      const bool ok = c0w + 32 * q + lane < trips;
       const bool gt = ok && rule.gt(kq[q]), eq = ok && rule.eq(kq[q]);
       const unsigned eqb = __ballot_sync(0xffffffffu, eq);
       const bool keep = gt || (eq && eq_base + (uint32_t)__popc(eqb & below) < need);
       const unsigned keepb = __ballot_sync(0xffffffffu, keep);
       if (keep) {
         const uint32_t pos = sel_base + (uint32_t)__popc(keepb & below);
-        if (pos < (uint32_t)p.k) out[pos] = c0 + s0 + j;
+        if (pos < (uint32_t)p.k) out[pos] = c0 + (int)iq[q];
       }
       sel_base += (uint32_t)__popc(keepb);
       eq_base += (uint32_t)__popc(eqb);
@@ -482,36 +604,39 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
 
 }  // namespace
 
-size_t topk_smem_bytes(int chunk) { return (size_t)chunk * 4 + sizeof(TkShared); }
+size_t topk_smem_bytes(int) { return sizeof(TkShared); }
+
+
+// Clusters of c CTAs (c = 1 .. 16) resident at once on a 152-SM GB300 with one or two 512-thread CTAs
+// per SM (cudaOccupancyMaxActiveClusters; a cluster's CTAs share one GPC).
+constexpr int kClustersPerWave[2][kTopkMaxCluster] = {
+    {152, 76, 46, 36, 28, 23, 15, 15, 15, 13, 8, 8, 7, 7, 7, 7},
+    {304, 152, 97, 74, 58, 46, 38, 36, 30, 28, 23, 23, 19, 14, 14, 14}};
 
 // Cluster size and chunk for rows of num_cols positions: every candidate size 1 .. 8 whose chunk fits
-// (9 .. 16 only for rows longer than 8 full chunks), scored by waves x per-CTA time, the latter fitted
-// to measured sweeps on GB300 (about 4 us fixed, 0.5 ns per position of the chunk for its four passes,
-// 3.5 us for the cluster-wide exchanges of a cluster of more than one CTA); ties keep the smaller
-// cluster.  When some size keeps every CTA on an SM of its own, only such sizes are considered: the
-// kernel is issue-bound, so two CTAs sharing an SM run at about half speed (B = 32 x 32768: 4-CTA
-// clusters 12.4 us, 8-CTA clusters 13.1 us).
+// (16 for rows longer than 8 full chunks), scored as full rows (one row per cluster) by waves x
+// per-wave time: a fixed part, a part per position of the chunk times the CTAs sharing an SM, and the
+// cluster-wide exchanges of a cluster of more than one CTA (fitted to measured sweeps on GB300); ties
+// keep the smaller cluster.  Chunks are multiples of kTopkChunkAlign positions (every warp a segment
+// of whole 128-entry steps).
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk) {
   double best_t = 0;
   int best_c = 0, best_chunk = 0;
   const bool long_rows = num_cols > kTopkPortableCluster * kTopkMaxChunk;
-  bool one_per_sm = false;  // some admissible size puts at most one CTA on each SM
-  for (int c = 1; c <= kTopkPortableCluster && forced_csize == 0 && !long_rows; ++c) {
-    const int ch = ((num_cols + c - 1) / c + 511) / 512 * 512;
-    if (ch <= kTopkMaxChunk && (long long)batch * c <= sm_count) one_per_sm = true;
-  }
+  auto chunk_for = [&](int c) { return ((num_cols + c - 1) / c + kTopkChunkAlign - 1) / kTopkChunkAlign * kTopkChunkAlign; };
   for (int c = 1; c <= kTopkMaxCluster; ++c) {
     if (forced_csize > 0 && c != forced_csize) continue;
-    if (forced_csize == 0 && c > kTopkPortableCluster && !long_rows) continue;
-    if (one_per_sm && (long long)batch * c > sm_count) continue;
-    const int ch = ((num_cols + c - 1) / c + 511) / 512 * 512;
+    if (forced_csize == 0 && c > kTopkPortableCluster && (!long_rows || c != kTopkMaxCluster)) continue;
+    const int ch = chunk_for(c);
     if (ch > kTopkMaxChunk) continue;
     if (forced_csize == 0 && c > 1 && (size_t)(c - 1) * ch >= (size_t)num_cols) continue;  // no empty CTA
     const size_t smem = topk_smem_bytes(ch) + 1024;
-    int cps = (int)((228u * 1024u) / smem);
-    cps = cps < 1 ? 1 : cps > 2 ? 2 : cps;  // two CTAs of 512 threads at most (launch bounds)
-    const double waves = ceil((double)batch * c / ((double)sm_count * cps));
-    const double t = waves * (4.0 + 0.5e-3 * ch + (c > 1 ? 3.5 : 0.0));
+    const int cps = smem * 2 <= 228u * 1024u ? 2 : 1;  // two CTAs of 512 threads at most (launch bounds)
+    const int per_wave = std::max(1, kClustersPerWave[cps - 1][c - 1] * sm_count / 152);
+    const int waves = (batch + per_wave - 1) / per_wave;
+    const int resident = batch < per_wave ? batch : per_wave;          // clusters in a full wave
+    const int sharing = (long long)resident * c > sm_count ? 2 : 1;    // CTAs per SM in that wave
+    const double t = waves * (kTkFixedUs + kTkPosUs * ch * sharing + (c > 1 ? kTkClusterUs : 0.0));
     if (best_c == 0 || t < best_t - 1e-9) {
       best_t = t;
       best_c = c;
@@ -543,13 +668,19 @@ cudaError_t configure_topk(int dev) {
   return cudaSuccess;
 }
 
-cudaError_t launch_topk(const TopkParams& p, int batch, cudaStream_t stream) {
+cudaError_t launch_topk(const TopkParams& p_in, int batch, cudaStream_t stream) {
   if (batch == 0) return cudaSuccess;
+  if (p_in.chunk <= 0 || p_in.chunk % kTopkChunkAlign != 0 || p_in.chunk > kTopkMaxChunk || p_in.csize < 1 ||
+      p_in.csize > kTopkMaxCluster)
+    return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   e = configure_topk(dev);
   if (e != cudaSuccess) return e;
+  TopkParams p = p_in;
+  p.batch = batch;
+  p.pack = p.csize > 1 && (p.csize & (p.csize - 1)) == 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * p.csize));
   cfg.blockDim = dim3(kTkThreads);

@@ -202,7 +202,7 @@ def test_topk_select_argument_checks_without_cuda(lib):
     assert call(D(4, 0, 1000, 8, 0), *ok) == 1                              # no positions
     assert call(D(4, 1000, 1000, 8, 17), *ok) == 1                          # cluster of 17 CTAs
     assert call(D(4, 1000, 1000, 4096, 0), *ok) == 2                        # k beyond 2048
-    assert call(D(4, 16 * 49152 + 1, 16 * 49152 + 1, 512, 0), *ok) == 2     # row too long
+    assert call(D(4, 16 * 65536 + 1, 16 * 65536 + 1, 512, 0), *ok) == 2     # row too long
     assert call(D(0, 1000, 1000, 512, 0), None, None, None, None, None) == 0   # empty batch: nothing to do
 
 
@@ -214,14 +214,14 @@ def _topk_plan(lib, B, n, k=512, forced=0, sms=152):
 
 
 @pytest.mark.parametrize("B,n", [(1, 256), (1, 8192), (32, 32768), (80, 131072), (96, 464028), (128, 65536),
-                                 (4, 786432), (7, 1000)])
+                                 (4, 786432), (2, 1048576), (7, 1000)])
 def test_topk_plan_shapes_cover_the_row(lib, B, n):
     st, c, ch = _topk_plan(lib, B, n)
     assert st == 0
-    assert 1 <= c <= 16 and ch % 512 == 0 and 512 <= ch <= 49152
+    assert 1 <= c <= 16 and ch % 2048 == 0 and 2048 <= ch <= 65536
     assert c * ch >= n                       # every position has a CTA
     assert c == 1 or (c - 1) * ch < n         # no CTA of an automatic choice is empty
-    assert (c > 8) == (n > 8 * 49152)         # clusters past the portable size only for long rows
+    assert (c > 8) == (n > 8 * 65536)         # clusters past the portable size only for long rows
 
 
 def test_topk_plan_keeps_one_cta_per_sm_when_it_can(lib):
@@ -236,7 +236,7 @@ def test_topk_plan_fixed_and_rejected(lib):
     assert _topk_plan(lib, 8, 20000, forced=3)[:2] == (0, 3)
     assert _topk_plan(lib, 8, 20000, forced=16)[:2] == (0, 16)   # kept as given, even with empty CTAs
     assert _topk_plan(lib, 8, 100000, forced=1)[0] == 2          # one CTA cannot hold 100000 positions
-    assert _topk_plan(lib, 8, 786433)[0] == 2                    # longer than 16 chunks
+    assert _topk_plan(lib, 8, 1048577)[0] == 2                   # longer than 16 chunks
     assert _topk_plan(lib, 8, 1000, k=4096)[0] == 2
     assert _topk_plan(lib, 8, 1000, forced=17)[0] == 1
     assert _topk_plan(lib, 8, 1000, sms=0)[0] == 1

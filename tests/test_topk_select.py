@@ -82,7 +82,7 @@ def test_padded_row_stride():
 
 
 @pytest.mark.parametrize("B,n,k", [(32, 32768, 512), (80, 131072, 512), (1, 8192, 512), (4, 393216, 2048),
-                                   (3, 524288, 512), (2, 786432, 1024)])
+                                   (3, 524288, 512), (2, 786432, 1024), (1, 1048576, 2048)])
 def test_decode_sizes(B, n, k):
     s = wl.make_indexer_scores(B, n, seed=B, device=DEV, pattern="relu")
     g = torch.Generator(device="cpu").manual_seed(B)
@@ -151,3 +151,16 @@ def test_bins_taken_whole(csize):
     s = torch.from_numpy(np.stack(rows)).to(DEV)
     lens = torch.full((len(rows),), n, dtype=torch.int32, device=DEV)
     _check(s, lens, k, cluster_ctas=csize)
+
+
+@pytest.mark.parametrize("csize", [0, 4, 16])
+def test_ragged_rows_share_clusters(csize):
+    # log-uniform lengths: most rows need one CTA and share a cluster with other rows, a few need several
+    B, n = 48, 200000
+    g = torch.Generator(device="cpu").manual_seed(12)
+    u = torch.rand(B, generator=g, dtype=torch.float64)
+    lens = (64 * (n / 64) ** u).floor().to(torch.int32)
+    lens[0] = n
+    lens[1] = 0
+    s = wl.make_indexer_scores(B, n, seed=12, device=DEV)
+    _check(s, lens.to(DEV), 512, cluster_ctas=csize)
