@@ -736,10 +736,13 @@ def main():
         import torch
         from sparse_mla_decode_paged_gb300 import api
         from sparse_mla_decode_paged_gb300 import workloads as wl
-        w = wl.make_workload(wl.CONFIGS[args.workload], device="cuda")
-        scores = wl.make_indexer_scores(w.B, int(w.seq_lens.max().item()), seed=5000, device="cuda")
+        # the workload's lengths (the same draw as its decode inputs) and score rows; no cache
+        spec = wl.CONFIGS[args.workload]
+        lens = torch.tensor(wl.draw_context_lengths(spec, wl._gen("cuda", spec.seed), "cuda"),
+                            dtype=torch.int32, device="cuda")
+        scores = wl.make_indexer_scores(spec.B, int(lens.max().item()), seed=5000, device="cuda")
         for _ in range(args.single):
-            api.sparse_mla_topk_select(scores, w.seq_lens, w.topk_idx.shape[1])
+            api.sparse_mla_topk_select(scores, lens, spec.topk)
         torch.cuda.synchronize()
         return
     if args.single:
