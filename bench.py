@@ -341,6 +341,41 @@ class Bench:
         barrier(world)
         return reduce_max(e0.elapsed_time(e1) / 1e3, world)
 
+    def replay_stats(self, fn, n_replays: int = 24, calls: int = 0):
+        """Per-call time of each of n_replays replays of one graph of `calls` calls (default: one call per
+        rotating input set, at most 64), each replay bracketed by its own events: (median, min, max) us."""
+        torch = self.torch
+        G = calls or min(self.R, 64)
+        g = self._graph(fn, 0, G)
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(n_replays):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3 / G)
+        return statistics.median(ts), min(ts), max(ts)
+
+    def single_calls(self, fn, n: int = 24):
+        """Eager calls (host launch included), each timed alone with events after the previous one
+        finished: median us."""
+        torch = self.torch
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        ts = []
+        for i in range(n):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn(i)
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
     def e2e(self, steps: int, warmup: int):
         """End to end through the public API with host buffers: every step copies its inputs from pinned
         host memory to the device, runs the decode call and reads out + lse back to pinned host memory.
@@ -440,6 +475,11 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
     us = t * 1e6 / steps
     ts = b.timed(b.split_only, steps, warmup)
     us_split = ts * 1e6 / steps
+    # other views of the same call: the median over graph replays (rotating inputs), the same with one
+    # input set replayed (warm L2: labelled, not the metric), and eager single calls (host launch included)
+    med, lo, hi = b.replay_stats(b.call)
+    warm, _, _ = b.replay_stats(lambda i: b.call(0), calls=16)
+    single = b.single_calls(b.call)
     gbs = b.bytes_per_call / (us * 1e-6) / 1e9
     b.append_setup()
     ta = b.timed(b.append_only, steps, warmup)
@@ -461,6 +501,10 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
            "roofline_frac_call": round(gbs / peak_gbs, 4),
            "roofline_frac_split_kernel": round(b.bytes_per_call / (us_split * 1e-6) / 1e9 / peak_gbs, 4),
            "rotations": b.R,
+           "graph_replays": {"replays": 24, "calls_per_replay": min(b.R, 64), "median_us_per_call": round(med, 3),
+                             "min": round(lo, 3), "max": round(hi, 3)},
+           "warm_l2_us_per_call": round(warm, 3),
+           "single_call_us": round(single, 3),
            "kv_append": {"tokens": b.w0.B, "us_per_call": round(us_app, 3), "algorithmic_bytes": b.app_bytes,
                          "gbs": round(b.app_bytes / (us_app * 1e-6) / 1e9, 1)},
            "topk_select": topk}
