@@ -21,15 +21,18 @@ def _lib():
 
 
 def _ptr(t: Optional[torch.Tensor]):
-    return C.c_void_p(t.data_ptr()) if t is not None else C.c_void_p(0)
+    """Device address for a void* argument (the library's argument types convert a plain int)."""
+    return t.data_ptr() if t is not None else None
 
 
 def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return C.c_void_p(s.cuda_stream)
+    return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
 
 
 def _need(t: torch.Tensor, name: str, dtype, ndim: int):
+    # the common case in one expression; the checks below only name what is wrong
+    if type(t) is torch.Tensor and t.is_cuda and t.dtype is dtype and t.dim() == ndim and t.is_contiguous():
+        return
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
@@ -54,6 +57,25 @@ def dims_of(q, kv_cache, block_table, topk_idx, nsplit: int = 0, heads_per_cta: 
     """Shapes of a call; several queries per request when q has a multiple of block_table's rows."""
     return make_dims(q.shape[0], q.shape[1], topk_idx.shape[1], block_table.shape[1], kv_cache.shape[0], nsplit,
                      heads_per_cta, q.shape[0] // block_table.shape[0], merge)
+
+
+# Decode dims by call shape and device, with the split count the library's scheduler chose filled in: a
+# call with the same shapes as an earlier one reuses them (the library reads dims, never writes them).
+_DECODE_DIMS = {}
+
+
+def _decode_dims(q, kv_cache, block_table, topk_idx, nsplit: int, heads_per_cta: int, merge: int) -> SmlaDims:
+    key = (q.shape, kv_cache.shape[0], block_table.shape, topk_idx.shape[1], nsplit, heads_per_cta, merge,
+           q.device.index)
+    d = _DECODE_DIMS.get(key)
+    if d is None:
+        d = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta, merge)
+        if nsplit == 0:
+            d.nsplit = plan(d, q.device.index).nsplit
+        if len(_DECODE_DIMS) > 256:
+            _DECODE_DIMS.clear()
+        _DECODE_DIMS[key] = d
+    return d
 
 
 def plan_for(dims: SmlaDims, sm_count: int) -> SmlaPlan:
@@ -102,21 +124,18 @@ def sparse_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torc
     """out bf16 [B,H,512], lse fp32 [B,H].  nsplit = 0, heads_per_cta = 0 and merge = MERGE_AUTO let the
     library's scheduler choose."""
     _check_inputs(q, kv_cache, block_table, topk_idx, seq_lens)
-    B, H = q.shape[0], q.shape[1]
-    dims = dims_of(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta, merge)
-    if nsplit == 0:
-        nsplit = plan(dims, q.device.index).nsplit
-        dims.nsplit = nsplit
+    dims = _decode_dims(q, kv_cache, block_table, topk_idx, nsplit, heads_per_cta, merge)
     if out is None:
-        out = torch.empty((B, H, D_LATENT), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((q.shape[0], q.shape[1], D_LATENT), dtype=torch.bfloat16, device=q.device)
     if lse is None:
-        lse = torch.empty((B, H), dtype=torch.float32, device=q.device)
+        lse = torch.empty((q.shape[0], q.shape[1]), dtype=torch.float32, device=q.device)
     if workspace is None:
-        workspace = alloc_workspace(dims, nsplit, q.device)
-    check("sparse_mla_decode", _lib().sparse_mla_decode(
-        C.byref(dims), _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(topk_idx), _ptr(seq_lens),
-        C.c_float(sm_scale), _ptr(out), _ptr(lse), _ptr(workspace), C.c_size_t(workspace.numel()),
-        _stream(stream)))
+        workspace = alloc_workspace(dims, dims.nsplit, q.device)
+    st = _lib().sparse_mla_decode(
+        dims, q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(), topk_idx.data_ptr(), seq_lens.data_ptr(),
+        sm_scale, out.data_ptr(), lse.data_ptr(), workspace.data_ptr(), workspace.numel(), _stream(stream))
+    if st != 0:
+        check("sparse_mla_decode", st)
     return out, lse
 
 

@@ -49,21 +49,55 @@ int check_inputs(const void* q, const void* kv, const int32_t* bt, const int32_t
   return SMLA_OK;
 }
 
+constexpr int kMaxDevices = 64;
+
+// SM count of the current device (queried once per device, then read from a per-device slot).
 int sm_count_of_current_device(int* sms) {
+  static std::atomic<int> cached[kMaxDevices];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) {
+    const int c = cached[dev].load(std::memory_order_relaxed);
+    if (c > 0) {
+      *sms = c;
+      return SMLA_OK;
+    }
+  }
   if (cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return SMLA_ERR_CUDA;
+  if (dev >= 0 && dev < kMaxDevices) cached[dev].store(*sms, std::memory_order_relaxed);
   return SMLA_OK;
 }
 
-// The scheduler's plan for dims with nsplit fixed (> 0) or chosen (0), on the current device.
+bool same_dims(const smla_dims& a, const smla_dims& b) {
+  return a.batch == b.batch && a.num_heads == b.num_heads && a.topk == b.topk && a.page_size == b.page_size &&
+         a.max_pages_per_seq == b.max_pages_per_seq && a.d_latent == b.d_latent && a.d_rope == b.d_rope &&
+         a.nsplit == b.nsplit && a.num_pages == b.num_pages && a.heads_per_cta == b.heads_per_cta &&
+         a.queries_per_request == b.queries_per_request && a.merge == b.merge;
+}
+
+// The scheduler's plan for dims with nsplit fixed (> 0) or chosen (0), on the current device.  The
+// plan of the last call on this host thread is kept: a call with the same dims on a device with the
+// same SM count reuses it.
 int plan_on_current_device(const smla_dims* dims, int nsplit, smla_plan* plan) {
+  struct Last {
+    bool valid;
+    int sms;
+    smla_dims d;
+    smla_plan plan;
+  };
+  thread_local Last last{};
   int sms = 0;
   const int st = sm_count_of_current_device(&sms);
   if (st != SMLA_OK) return st;
   smla_dims d = *dims;
   d.nsplit = nsplit;
-  return sparse_mla_plan_for(&d, sms, plan);
+  if (last.valid && last.sms == sms && same_dims(last.d, d)) {
+    *plan = last.plan;
+    return SMLA_OK;
+  }
+  const int r = sparse_mla_plan_for(&d, sms, plan);
+  if (r == SMLA_OK) last = Last{true, sms, d, *plan};
+  return r;
 }
 
 SplitParams make_params(const smla_dims* d, int nsplit, int nh, const void* q, const void* kv, const int32_t* bt,
