@@ -105,9 +105,9 @@ def test_selected_lists_feed_the_decode():
 
 
 @pytest.mark.parametrize("csize", [1, 4])
-def test_one_coarse_bin_overflows_the_candidate_list(csize):
-    # every score in [1, 1.25): one coarse bin (same exponent and top mantissa bits), distinct keys, so
-    # more candidates than a CTA lists and the refinement scans the whole chunk
+def test_one_top_digit_bin_overflows_the_lists(csize):
+    # every score in [1, 1.25): one top-digit bin (same exponent and top mantissa bits), distinct keys,
+    # so more candidates than a warp lists and the later steps read the segment again
     g = torch.Generator(device=DEV).manual_seed(8)
     s = 1.0 + 0.2499 * torch.rand((3, 40000), generator=g, device=DEV)
     s[2, ::3] = 1.125                         # plus heavy ties inside that bin
@@ -116,7 +116,8 @@ def test_one_coarse_bin_overflows_the_candidate_list(csize):
 
 
 @pytest.mark.parametrize("scale", [1e-9, 1e-6, 1e7, 3e38])
-def test_scores_outside_the_coarse_window(scale):
+def test_scores_at_extreme_magnitudes(scale):
+    # tiny, huge and near-overflow scores: every exponent lands in its own top-digit bins
     s = wl.make_indexer_scores(4, 6000, seed=9, device=DEV) * scale
     lens = torch.tensor([6000, 5000, 3000, 600], dtype=torch.int32, device=DEV)
     for c in (1, 2):
@@ -135,9 +136,9 @@ def _row(parts, n):
 
 @pytest.mark.parametrize("csize", [1, 3])
 def test_bins_taken_whole(csize):
-    # rows where the k-th entry closes a coarse bin or a refinement digit exactly, so the select stops
+    # rows where the k-th entry closes a top-digit bin or a refinement digit exactly, so the select stops
     # early and keeps "everything from a bin boundary up": positive, negative, infinite and signed-zero
-    # boundaries, and a digit boundary inside one coarse bin
+    # boundaries, and a digit boundary inside one top-digit bin
     n, k = 6000, 512
     rows = [
         _row([(k, 10.0), (0, 1.0)], n),
