@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from oracle import topk_select_oracle as T
-from sparse_mla_decode_paged_gb300 import api
+from sparse_mla_decode_paged_gb300 import _native, api
 from sparse_mla_decode_paged_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -176,3 +176,33 @@ def test_more_rows_than_the_length_cache():
     lens[-1] = n
     s = wl.make_indexer_scores(B, n, seed=13, device=DEV)
     _check(s, lens.to(DEV), k, cluster_ctas=2)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_shapes(case):
+    # seeded random shapes: batch, row width, stride (aligned or not), k, cluster size, score pattern and
+    # lengths (including 0, k, k + 1 and out-of-range values, which the oracle clamps the same way)
+    rng = np.random.default_rng(1000 + case)
+    B = int(rng.integers(1, 40))
+    n = int(rng.integers(1, 60000))
+    k = int(rng.choice([1, 7, 64, 512, 2048]))
+    csize = int(rng.choice([0, 1, 2, 3, 4, 8, 16]))
+    pattern = wl.SCORE_PATTERNS[case % len(wl.SCORE_PATTERNS)]
+    pad = int(rng.choice([0, 1, 3, 64]))
+    base = wl.make_indexer_scores(B, n + pad + 1, seed=2000 + case, device=DEV, pattern=pattern)
+    s = base[:, 1:n + 1] if pad % 2 else base[:, :n]
+    lens = rng.integers(0, n + 1, size=B)
+    for i, v in enumerate([0, k, k + 1, n, n + 5, -3]):
+        if i < B:
+            lens[i] = v
+    lens = torch.from_numpy(lens.astype(np.int32)).to(DEV)
+    try:
+        got = api.sparse_mla_topk_select(s, lens, k, cluster_ctas=csize)
+    except _native.SmlaError as e:
+        # a fixed cluster size whose chunk would exceed the per-CTA limit is refused on the host
+        assert csize > 0 and e.status == 2, e
+        return
+    torch.cuda.synchronize()
+    ref = T.topk_select(s.cpu().numpy(), lens.cpu().numpy(), k)
+    bad = np.flatnonzero(np.any(got.cpu().numpy() != ref, axis=1))
+    assert bad.size == 0, f"case {case} (B={B}, n={n}, k={k}, csize={csize}, {pattern}): rows {bad[:8].tolist()}"
