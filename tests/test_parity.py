@@ -195,12 +195,13 @@ def _sample(B, n, seed):
     return sorted(rng.choice(B, size=min(n, B), replace=False).tolist())
 
 
-def _decode_rows(w, nsplit=0, heads_per_cta=0):
+def _decode_rows(w, nsplit=0, heads_per_cta=0, merge=api.MERGE_AUTO):
     """Decode that also returns the rows its split kernel loaded; the row buffer starts as a sentinel
     no entry can produce, so an entry the kernel never resolved shows up."""
     rows = torch.full(tuple(w.topk_idx.shape), -7, dtype=torch.int64, device=DEV)
     out, lse, rows = api.sparse_mla_decode_rows(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens,
-                                                w.sm_scale, nsplit=nsplit, heads_per_cta=heads_per_cta, rows=rows)
+                                                w.sm_scale, nsplit=nsplit, heads_per_cta=heads_per_cta, rows=rows,
+                                                merge=merge)
     torch.cuda.synchronize()
     return out, lse, rows
 
@@ -243,3 +244,27 @@ def test_full_size_configs_sampled(name):
     finally:
         del w
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("case", range(10))
+def test_random_shapes(case):
+    # seeded random shapes through the decode with its rows: batch, heads, top-k, ragged lengths (some
+    # shorter than top-k, some of one token), partition count, head-group size and merge path
+    rng = np.random.default_rng(3000 + case)
+    H = int(rng.choice([16, 32, 64, 128]))
+    B = int(rng.integers(1, 7))
+    topk = int(rng.choice([1, 33, 128, 200, 512, 1000, 2048]))
+    ctx = [int(rng.choice([1, int(rng.integers(2, topk + 2)), int(rng.integers(topk, 9000))])) for _ in range(B)]
+    nh = int(rng.choice([0, 16, 32, 64]))
+    nh = nh if nh <= H else 0
+    nsplit = int(rng.choice([0, 1, 2, 3, 4, 8, 16]))
+    merge = int(rng.choice([api.MERGE_AUTO, api.MERGE_KERNEL, api.MERGE_FUSED]))
+    w = _custom(B=B, H=H, topk=topk, ctx=ctx, seed=3100 + case, outlier_channels=int(rng.integers(0, 3)))
+    try:
+        out, lse, rows = _decode_rows(w, nsplit=nsplit, heads_per_cta=nh, merge=merge)
+    except Exception as e:
+        # a merge inside the kernel that no launch shape of these dims allows is refused on the host
+        assert merge == api.MERGE_FUSED and "UNSUPPORTED" in str(e), e
+        return
+    assert np.array_equal(rows.cpu().numpy(), oracle_rows(w)), f"case {case}"
+    compare(out, lse, *oracle_on(w))
