@@ -81,6 +81,7 @@ struct TopkParams {
   int vec4;                   // scores 16-byte aligned and stride % 4 == 0: 16-byte loads
   int batch;                  // rows (set by launch_topk)
   int pack;                   // csize a power of two > 1: rows packed into clusters by their chunk count
+  int pre8;                   // the top byte of every key kept in shared memory (set by launch_topk)
 };
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk);
 size_t topk_smem_bytes(int chunk);

@@ -9,17 +9,19 @@
 // thread-block cluster.  With a power-of-two cluster size the rows are packed: a row of u chunks takes
 // an aligned group of u' CTAs (u' = u rounded up to a power of two), the groups ordered by size, so a
 // cluster holds one long row or several short ones and a ragged batch does not give every row a whole
-// cluster.  Nothing per position stays in shared memory (so two CTAs fit on an SM whatever the chunk):
-// each warp streams its contiguous segment of the chunk twice, once from HBM (16-byte streaming loads)
-// and once more from L2, as 32-bit order keys.  Selection is a radix select in 11-, 11- and 10-bit
+// cluster.  Each warp streams its contiguous segment of the chunk from HBM once (16-byte streaming
+// loads) as 32-bit order keys; shared memory keeps at most one byte per position (the key's top byte,
+// when two CTAs still fit on an SM with it), so long chunks cost no occupancy.  Selection is a radix
+// select in 11-, 11- and 10-bit
 // digits: every decision is taken identically by every CTA of the row from digit histograms that each
 // CTA adds into all the row's CTAs' shared memory (remote reductions) before a cluster barrier, so
 // after the barrier each CTA reads only its own shared memory, no CTA leads and nothing waits on a
 // flag:
 //   1. the top digit (sign, exponent, two mantissa bits), histogrammed on the first pass: digits above
 //      the one holding the k-th key are kept whole, digits below dropped;
-//   2. the second pass lists, per warp and in position order, the entries at or above that digit (the
-//      kept-for-sure entries and the candidates) with their keys;
+//   2. each warp lists, in position order, the entries at or above that digit (the kept-for-sure
+//      entries and the candidates) with their keys: from the key bytes, only the positions whose top
+//      byte can reach the digit are read again (from L2); without them the whole segment is;
 //   3. the candidates are refined digit by digit from the lists; the select stops as soon as a
 //      digit's bin is kept whole.
 // The outcome is one threshold key; per-warp counts over the lists, the counts of the row's lower CTAs
@@ -51,7 +53,7 @@ constexpr int kTkRowsCached = 4;       // row lengths a thread keeps while the r
 // launch-shape model of topk_plan: us per wave, per chunk position (per CTA sharing the SM), per cluster
 constexpr double kTkFixedUs = 4.0, kTkPosUs = 0.25e-3, kTkClusterUs = 3.0;
 
-struct TkShared {
+struct alignas(16) TkShared {
   // row-wide digit histograms, accumulated by remote reductions from every CTA of the row: the top
   // digit in [0], the second in [1], the last in [0] again (cleared once the top digit is picked)
   uint32_t hsum[2][kTkBins];
@@ -198,6 +200,8 @@ __device__ __forceinline__ uint32_t key_at(const float* row, int i) {
 __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TkShared& s = *reinterpret_cast<TkShared*>(smem_raw);
+  // with p.pre8: the top 8 bits of every position's key, after TkShared
+  uint8_t* const pre8 = smem_raw + sizeof(TkShared);
   const int cs = p.csize;
   const int rank = cs > 1 ? (int)cluster_ctarank() : 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -341,14 +345,23 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
         for (int u = 0; u < kTkLoadUnroll; ++u) {
           const int j = base + 32 * u + lane;
           if (j < n4) {
-            atomicAdd(h + (order_key(v[u].x) >> 21), 1u);
-            atomicAdd(h + (order_key(v[u].y) >> 21), 1u);
-            atomicAdd(h + (order_key(v[u].z) >> 21), 1u);
-            atomicAdd(h + (order_key(v[u].w) >> 21), 1u);
+            const uint32_t k0 = order_key(v[u].x), k1 = order_key(v[u].y), k2 = order_key(v[u].z),
+                           k3 = order_key(v[u].w);
+            atomicAdd(h + (k0 >> 21), 1u);
+            atomicAdd(h + (k1 >> 21), 1u);
+            atomicAdd(h + (k2 >> 21), 1u);
+            atomicAdd(h + (k3 >> 21), 1u);
+            if (p.pre8)  // the four top bytes, in position order
+              *reinterpret_cast<uint32_t*>(pre8 + s0 + 4 * j) =
+                  __byte_perm(__byte_perm(k0, k1, 0x0073), __byte_perm(k2, k3, 0x0073), 0x5410);
           }
         }
       }
-      if (lane < (s_len & 3)) atomicAdd(h + (key_at(src, (n4 << 2) + lane) >> 21), 1u);  // scalar tail
+      if (lane < (s_len & 3)) {  // scalar tail
+        const uint32_t kk = key_at(src, (n4 << 2) + lane);
+        atomicAdd(h + (kk >> 21), 1u);
+        if (p.pre8) pre8[s0 + (n4 << 2) + lane] = (uint8_t)(kk >> 24);
+      }
     } else {
       for (int base = 0; base < s_len; base += 32 * kTkLoadUnroll) {
         uint32_t v[kTkLoadUnroll];
@@ -359,7 +372,11 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
         }
 #pragma unroll
         for (int u = 0; u < kTkLoadUnroll; ++u)
-          if (base + 32 * u + lane < s_len) atomicAdd(h + (order_key(v[u]) >> 21), 1u);
+          if (base + 32 * u + lane < s_len) {
+            const uint32_t kk = order_key(v[u]);
+            atomicAdd(h + (kk >> 21), 1u);
+            if (p.pre8) pre8[s0 + base + 32 * u + lane] = (uint8_t)(kk >> 24);
+          }
       }
     }
   }
@@ -408,13 +425,91 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
       }
     my_cnt += total;
   };
-  if (active) {
-    // order_key(x) >= prefix as one compare on the raw bits x: with prefix in the positive half, x read
-    // as a signed integer reaches prefix's magnitude bits; otherwise x (unsigned) is at most ~prefix
-    const bool pos_lo = (prefix >> 31) != 0;
-    const int lo_s = (int)(prefix & 0x7FFFFFFFu);
-    const uint32_t lo_u = ~prefix;
-    auto reach = [&](uint32_t x) { return pos_lo ? (int)x >= lo_s : x <= lo_u; };
+  // order_key(x) >= prefix as one compare on the raw bits x: with prefix in the positive half, x read
+  // as a signed integer reaches prefix's magnitude bits; otherwise x (unsigned) is at most ~prefix
+  const bool pos_lo = (prefix >> 31) != 0;
+  const int lo_s = (int)(prefix & 0x7FFFFFFFu);
+  const uint32_t lo_u = ~prefix;
+  auto reach = [&](uint32_t x) { return pos_lo ? (int)x >= lo_s : x <= lo_u; };
+  bool streamed = !p.pre8;  // the listing reads the whole segment again (no key bytes, or too many candidates)
+  if (active && p.pre8) {
+    // candidates: positions whose top key byte reaches prefix's (a superset of the entries >= prefix),
+    // listed in position order; lane l takes 16 consecutive positions per step
+    // byte b >= t (t = prefix's top byte) four bytes at a time: (b & 0x7F) + 0x80 - (t & 0x7F) sets the
+    // byte's top bit exactly when b & 0x7F >= t & 0x7F (no carry leaves the byte); combined with b's own
+    // top bit by AND when t >= 0x80 (b must be at least 0x80 too) and by OR otherwise
+    const uint32_t t8 = prefix >> 24;
+    const uint32_t add = (0x80u - (t8 & 0x7Fu)) * 0x01010101u;
+    const bool t_hi = t8 >= 0x80u;
+    auto reach4 = [&](uint32_t w) {
+      const uint32_t y = (w & 0x7F7F7F7Fu) + add;
+      return (t_hi ? (y & w) : (y | w)) & 0x80808080u;
+    };
+    // the four flags of a word (bits 7, 15, 23, 31) as a nibble
+    auto nibble = [](uint32_t y) { return (((y >> 7) * 0x00204081u) >> 21) & 0xFu; };
+    uint32_t ncand = 0;
+    for (int j0 = 0; j0 < s_len; j0 += 512) {  // warp-uniform
+      const int j = j0 + 16 * lane;
+      uint32_t y[4] = {0u, 0u, 0u, 0u};
+      if (j < s_len) {
+        const uint4 b = *reinterpret_cast<const uint4*>(pre8 + s0 + j);
+        y[0] = reach4(b.x);
+        y[1] = reach4(b.y);
+        y[2] = reach4(b.z);
+        y[3] = reach4(b.w);
+      }
+      if (!__any_sync(0xffffffffu, (y[0] | y[1] | y[2] | y[3]) != 0u)) continue;
+      uint32_t m = nibble(y[0]) | (nibble(y[1]) << 4) | (nibble(y[2]) << 8) | (nibble(y[3]) << 12);
+      const int lim = s_len - j;  // bit i: position j + i is a candidate (positions below s_len only)
+      if (lim < 16) m &= lim > 0 ? (1u << lim) - 1u : 0u;
+      const uint32_t c = (uint32_t)__popc(m);
+      uint32_t incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const uint32_t total = __shfl_sync(0xffffffffu, incl, 31);
+      uint32_t at = ncand + incl - c;
+      while (m) {
+        const int i = __ffs(m) - 1;
+        m &= m - 1;
+        if (at < (uint32_t)kTkWarpList) li[at] = (uint16_t)(s0 + j + i);
+        ++at;
+      }
+      ncand += total;
+    }
+    __syncwarp();
+    if (ncand <= (uint32_t)kTkWarpList) {
+      // resolve the candidates (their scores from L2, 128 in flight per warp), keeping the entries >=
+      // prefix, compacted in place in position order
+      for (uint32_t b0 = 0; b0 < ncand; b0 += 128) {  // warp-uniform
+        uint32_t x[4], ix[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t c = b0 + 32 * q + lane;
+          ix[q] = c < ncand ? li[c] : 0u;
+          x[q] = c < ncand ? __ldg(reinterpret_cast<const unsigned int*>(row_src + c0) + ix[q]) : 0u;
+        }
+        __syncwarp();  // every candidate of this step is read before the compacted writes
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const bool hit = b0 + 32 * q + lane < ncand && reach(x[q]);
+          const unsigned hm = __ballot_sync(0xffffffffu, hit);
+          if (hit) {
+            const uint32_t at = my_cnt + (uint32_t)__popc(hm & below);
+            lk[at] = order_key(x[q]);
+            li[at] = (uint16_t)ix[q];
+          }
+          my_cnt += (uint32_t)__popc(hm);
+        }
+        __syncwarp();
+      }
+    } else {
+      streamed = true;
+    }
+  }
+  if (active && streamed) {
     if (p.vec4) {
       const int n4 = s_len >> 2;
       for (int base = 0; base < n4; base += 32 * kTkLoadUnroll) {  // warp-uniform
@@ -604,7 +699,11 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
 
 }  // namespace
 
-size_t topk_smem_bytes(int) { return sizeof(TkShared); }
+// One byte per position (the top 8 bits of its key) joins the shared memory when two CTAs still fit on
+// an SM with it.
+bool topk_key_bytes(int chunk) { return 2 * (sizeof(TkShared) + (size_t)chunk + 1024) <= 228u * 1024u; }
+
+size_t topk_smem_bytes(int chunk) { return sizeof(TkShared) + (topk_key_bytes(chunk) ? (size_t)chunk : 0); }
 
 
 // Clusters of c CTAs (c = 1 .. 16) resident at once on a 152-SM GB300 with one or two 512-thread CTAs
@@ -659,8 +758,9 @@ cudaError_t configure_topk(int dev) {
   if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_acquire)) return cudaSuccess;
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_relaxed)) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)topk_smem_bytes(kTopkMaxChunk));
+  size_t most = 0;  // the largest shared memory any chunk takes
+  for (int ch = kTopkChunkAlign; ch <= kTopkMaxChunk; ch += kTopkChunkAlign) most = std::max(most, topk_smem_bytes(ch));
+  cudaError_t e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)most);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
@@ -681,6 +781,7 @@ cudaError_t launch_topk(const TopkParams& p_in, int batch, cudaStream_t stream) 
   TopkParams p = p_in;
   p.batch = batch;
   p.pack = p.csize > 1 && (p.csize & (p.csize - 1)) == 0;
+  p.pre8 = topk_key_bytes(p.chunk);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * p.csize));
   cfg.blockDim = dim3(kTkThreads);
