@@ -47,7 +47,7 @@ constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkBins = 2048;          // 11-bit digits: key bits 31..21, then 20..10
 constexpr int kTkLastBins = 1024;      // the last digit: key bits 9..0
 constexpr int kTkLoadUnroll = 4;       // 16-byte (or 4-byte) loads in flight per thread
-constexpr int kTkWarpList = 512;       // entries listed per warp
+constexpr int kTkWarpList = 384;       // entries listed per warp (sized so that long chunks keep their key bytes)
 constexpr int kTkMaxClass = 4;         // packed row groups of 1, 2, 4, 8 or 16 CTAs
 constexpr int kTkRowsCached = 4;       // row lengths a thread keeps while the rows are packed
 // launch-shape model of topk_plan: us per wave, per chunk position (per CTA sharing the SM), per cluster
