@@ -12,11 +12,10 @@
 // cluster.  Each warp streams its contiguous segment of the chunk from HBM once (16-byte streaming
 // loads) as 32-bit order keys; shared memory keeps at most one byte per position (the key's top byte,
 // when two CTAs still fit on an SM with it), so long chunks cost no occupancy.  Selection is a radix
-// select in 11-, 11- and 10-bit
-// digits: every decision is taken identically by every CTA of the row from digit histograms that each
-// CTA adds into all the row's CTAs' shared memory (remote reductions) before a cluster barrier, so
-// after the barrier each CTA reads only its own shared memory, no CTA leads and nothing waits on a
-// flag:
+// select in 11-, 11- and 10-bit digits: every decision is taken identically by every CTA of the row
+// from digit histograms that each CTA adds into all the row's CTAs' shared memory (remote reductions)
+// before a cluster barrier, so after the barrier each CTA reads only its own shared memory, no CTA
+// leads and nothing waits on a flag:
 //   1. the top digit (sign, exponent, two mantissa bits), histogrammed on the first pass: digits above
 //      the one holding the k-th key are kept whole, digits below dropped;
 //   2. each warp lists, in position order, the entries at or above that digit (the kept-for-sure
