@@ -273,9 +273,9 @@ int sparse_mla_topk_select(const smla_topk_dims* dims, const float* scores, cons
  * sm_count SMs (host only, no CUDA call): clusters of *cluster_ctas CTAs,
  * each CTA holding *chunk_positions positions of one row (a multiple of 2048,
  * at most 65536, cluster_ctas x chunk_positions >= num_cols).  A row spans
- * at most one cluster; with a power-of-two cluster size, rows that need fewer
- * chunks than the cluster has CTAs share clusters (packed by their chunk
- * count on the device, from seq_lens).  dims->cluster_ctas > 0 is kept as
+ * at most one cluster; with a power-of-two cluster size and at most 2048
+ * rows, rows that need fewer chunks than the cluster has CTAs share clusters
+ * (packed by their chunk count on the device, from seq_lens).  dims->cluster_ctas > 0 is kept as
  * given.  Returns SMLA_ERR_INVALID_ARG for bad shapes or pointers,
  * SMLA_ERR_UNSUPPORTED when no shape fits. */
 int sparse_mla_topk_plan_for(const smla_topk_dims* dims, int32_t sm_count, int32_t* cluster_ctas,

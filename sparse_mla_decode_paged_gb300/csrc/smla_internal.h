@@ -71,6 +71,7 @@ constexpr int kTopkPortableCluster = 8;  // cluster sizes every launch supports
 constexpr int kTopkMaxCluster = 16;      // with the non-portable cluster size attribute (rows past 8 chunks)
 constexpr int kTopkMaxChunk = 65536;     // scores per CTA (chunk indexes are 16-bit)
 constexpr int kTopkChunkAlign = 2048;    // chunks are multiples of this (16 warps x 128-entry steps)
+constexpr int kTopkPackMaxRows = 2048;   // rows packed into clusters only for batches up to this size
 struct TopkParams {
   const float* scores;        // [batch][stride]
   const int32_t* seq_lens;    // [batch]

@@ -49,6 +49,7 @@ constexpr int kTkLoadUnroll = 4;       // 16-byte (or 4-byte) loads in flight pe
 constexpr int kTkWarpList = 384;       // entries listed per warp (sized so that long chunks keep their key bytes)
 constexpr int kTkMaxClass = 4;         // packed row groups of 1, 2, 4, 8 or 16 CTAs
 constexpr int kTkRowsCached = 4;       // row lengths a thread keeps while the rows are packed
+static_assert(kTkRowsCached * kTkThreads >= kTopkPackMaxRows, "every packed row's length fits the registers");
 // launch-shape model of topk_plan: us per wave, per chunk position (per CTA sharing the SM), per cluster
 constexpr double kTkFixedUs = 4.0, kTkPosUs = 0.25e-3, kTkClusterUs = 3.0;
 
@@ -216,8 +217,8 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
     raw_len = __ldg(p.seq_lens + row);
   } else {
     // groups in decreasing size, rows in index order within a size: group starts are multiples of
-    // their size, so no group crosses a cluster.  Every CTA reads all lengths once (the first
-    // kTkRowsCached per thread stay in registers for the search below).
+    // their size, so no group crosses a cluster.  Every CTA reads all lengths once into registers
+    // (packing is used for at most kTkRowsCached * kTkThreads rows).
     const int top = 31 - __clz(cs);
     if (tid <= kTkMaxClass) s.ncls[tid] = 0;
     if (tid == 0) s.row_found = -1;
@@ -227,18 +228,12 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
       const int b = i * kTkThreads + tid;
       lens_c[i] = b < p.batch ? __ldg(p.seq_lens + b) : 0;
     }
-    // length of row b = i * kTkThreads + tid (this thread's i-th row)
-    auto len_of = [&](int i, int b) {
-      int v = 0;
-#pragma unroll
-      for (int r = 0; r < kTkRowsCached; ++r)
-        if (r == i) v = lens_c[r];
-      return i < kTkRowsCached ? v : (b < p.batch ? __ldg(p.seq_lens + b) : 0);
-    };
     __syncthreads();
-    for (int b0 = 0, i = 0; b0 < p.batch; b0 += kTkThreads, ++i) {
-      const int b = b0 + tid;
-      const int len_b = len_of(i, b);
+#pragma unroll
+    for (int i = 0; i < kTkRowsCached; ++i) {
+      if (i * kTkThreads >= p.batch) break;  // block-uniform
+      const int b = i * kTkThreads + tid;
+      const int len_b = lens_c[i];
       const int c = b < p.batch ? len_class(p, len_b) : -1;
       for (int j = 0; j <= top; ++j) {
         const unsigned m = __ballot_sync(0xffffffffu, c == j);
@@ -264,9 +259,11 @@ __global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(TopkParams p) {
       grp.g0 = rank - sub;
       const uint32_t q = (g - my_off) >> my_cls;  // rank of the row among the rows of its class
       uint32_t seen = 0;
-      for (int b0 = 0, i = 0; b0 < p.batch; b0 += kTkThreads, ++i) {  // block-uniform trip count
-        const int b = b0 + tid;
-        const int len_b = len_of(i, b);
+#pragma unroll
+      for (int i = 0; i < kTkRowsCached; ++i) {
+        if (i * kTkThreads >= p.batch) break;  // block-uniform
+        const int b = i * kTkThreads + tid;
+        const int len_b = lens_c[i];
         const bool is = b < p.batch && len_class(p, len_b) == my_cls;
         const unsigned m = __ballot_sync(0xffffffffu, is);
         if (lane == 0) s.scan[warp] = (uint32_t)__popc(m);
@@ -779,7 +776,9 @@ cudaError_t launch_topk(const TopkParams& p_in, int batch, cudaStream_t stream) 
   if (e != cudaSuccess) return e;
   TopkParams p = p_in;
   p.batch = batch;
-  p.pack = p.csize > 1 && (p.csize & (p.csize - 1)) == 0;
+  // rows are packed by a pass over every length in every CTA: kept for batches whose lengths fit the
+  // CTA's registers (larger batches take one row per cluster)
+  p.pack = p.csize > 1 && (p.csize & (p.csize - 1)) == 0 && batch <= kTopkPackMaxRows;
   p.pre8 = topk_key_bytes(p.chunk);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(batch * p.csize));

@@ -167,10 +167,11 @@ def test_ragged_rows_share_clusters(csize):
     _check(s, lens.to(DEV), 512, cluster_ctas=csize)
 
 
-def test_more_rows_than_the_length_cache():
-    # 2100 rows packed into clusters of 2: each CTA reads every length (past the 4 x 512 it keeps in
-    # registers it reads them again) and finds its row among several 512-row rounds
-    B, n, k = 2100, 4096, 64
+@pytest.mark.parametrize("B", [2048, 2100])
+def test_many_rows(B):
+    # 2048 rows packed into clusters of 2 (each CTA reads every length and finds its row among four
+    # 512-row rounds); past 2048 rows every row takes a cluster of its own
+    n, k = 4096, 64
     g = torch.Generator(device="cpu").manual_seed(13)
     lens = torch.randint(0, n + 1, (B,), generator=g, dtype=torch.int32)
     lens[-1] = n
