@@ -289,6 +289,16 @@ class Bench:
         s = self.tk_sets[i % len(self.tk_sets)]
         self.api.sparse_mla_topk_select(s, self.tk_lens, self.tk_out.shape[1])
 
+    def topk_then_decode(self, i: int):
+        """A decode step's attention: the top-k selection over rotating score rows, then the decode of
+        rotating inputs reading the lists it just produced (a programmatic dependent of the selection)."""
+        s = self.tk_sets[i % len(self.tk_sets)]
+        w = self.sets[i % self.R]
+        tk = self.api.sparse_mla_topk_select(s, self.tk_lens, self.tk_out.shape[1])
+        self.api.sparse_mla_decode(w.q, self.cache, w.block_table, tk, w.seq_lens, w.sm_scale,
+                                   out=self.out, lse=self.lse, workspace=self.ws, nsplit=self.nsplit,
+                                   heads_per_cta=self.plan.heads_per_cta, merge=self.dims.merge)
+
     def launches_per_call(self) -> int:
         return 1 + (1 if self.nsplit > 1 and not self.plan.fused else 0)
 
@@ -505,11 +515,14 @@ def measure_config(name: str, device, steps: int, warmup: int, peak_gbs: float):
         b.topk_setup()
         tt = b.timed(b.topk_only, steps, warmup)
         us_tk = tt * 1e6 / steps
+        tp = b.timed(b.topk_then_decode, steps, warmup)
+        us_pipe = tp * 1e6 / steps
         topk = {"queries": b.w0.B, "positions": b.tk_cols, "k": b.tk_out.shape[1],
                 "scores": "standard normal float32", "rotating_sets": len(b.tk_sets),
                 "us_per_call": round(us_tk, 3), "algorithmic_bytes": b.tk_bytes,
                 "gbs": round(b.tk_bytes / (us_tk * 1e-6) / 1e9, 1),
-                "roofline_frac": round(b.tk_bytes / (us_tk * 1e-6) / 1e9 / peak_gbs, 4)}
+                "roofline_frac": round(b.tk_bytes / (us_tk * 1e-6) / 1e9 / peak_gbs, 4),
+                "then_decode_us_per_call": round(us_pipe, 3)}
     except Exception as e:  # a side measurement: keep the decode's numbers
         topk = {"error": repr(e)}
     res = {"us_per_call": round(us, 3), "split_kernel_us": round(us_split, 3), "nsplit": b.nsplit,
