@@ -50,7 +50,8 @@ constexpr int kTkWarpList = 384;       // entries listed per warp (sized so that
 constexpr int kTkMaxClass = 4;         // packed row groups of 1, 2, 4, 8 or 16 CTAs
 constexpr int kTkRowsCached = 4;       // row lengths a thread keeps while the rows are packed
 static_assert(kTkRowsCached * kTkThreads >= kTopkPackMaxRows, "every packed row's length fits the registers");
-// launch-shape model of topk_plan: us per wave, per chunk position (per CTA sharing the SM), per cluster
+// launch-shape model of topk_plan (round numbers, checked against sweeps): us per wave, per chunk
+// position (per CTA sharing the SM), per cluster
 constexpr double kTkFixedUs = 4.0, kTkPosUs = 0.25e-3, kTkClusterUs = 3.0;
 
 struct alignas(16) TkShared {
@@ -711,8 +712,9 @@ constexpr int kClustersPerWave[2][kTopkMaxCluster] = {
 // Cluster size and chunk for rows of num_cols positions: every candidate size 1 .. 8 whose chunk fits
 // (16 for rows longer than 8 full chunks), scored as full rows (one row per cluster) by waves x
 // per-wave time: a fixed part, a part per position of the chunk times the CTAs sharing an SM, and the
-// cluster-wide exchanges of a cluster of more than one CTA (fitted to measured sweeps on GB300); ties
-// keep the smaller cluster.  Chunks are multiples of kTopkChunkAlign positions (every warp a segment
+// cluster-wide exchanges of a cluster of more than one CTA (round constants, checked against measured
+// sweeps of every cluster size on GB300: the model's pick is the fastest measured size on each of the
+// decode workloads' shapes); ties keep the smaller cluster.  Chunks are multiples of kTopkChunkAlign positions (every warp a segment
 // of whole 128-entry steps).
 bool topk_plan(int batch, int num_cols, int sm_count, int forced_csize, int* csize, int* chunk) {
   double best_t = 0;
