@@ -28,6 +28,10 @@
 //   MMA issue          one elected lane of softmax warp 0, from unrolled issuers whose descriptors
 //                      are a base plus a compile-time offset: the 36 QK MMAs of a tile in one batch
 //                      (block b into score buffer b, the rope into block 0's), then the PV MMAs.
+//                      The issuing thread waits while the tensor core takes the MMAs (about as long
+//                      as they run), so in launches of one tile per CTA (kOneTile) gather warp 0,
+//                      which has no next tile to load, issues the QK instead, and every softmax warp
+//                      reads each score buffer as it completes.
 //   softmax (4 warps)  one token (TMEM lane) per thread, NH heads: scores accumulated from the score
 //                      buffers as they complete, lazy running max (a head's reference moves only
 //                      when a score exceeds it by more than 2^8; O and the row sums are then
@@ -224,7 +228,9 @@ struct Ctx {
 };
 
 // ------------------------------------------------------------------------------------------ gather
+template <int NH, bool kOneTile>
 __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
+  using C = Cfg<NH>;
   const SplitParams& p = *x.p;
   Misc& ms = *x.ms;
   const int gw = warp - kSoftWarps;
@@ -398,10 +404,37 @@ __device__ __forceinline__ void gather_role(const Ctx& x, int warp, int lane) {
     t4 = topk_load(i + 5);
   }
   if (range_bad) ms.range_err = 1;
+  if constexpr (kOneTile) {
+    if (gw == 0) {
+      // the tile's QK (one elected lane): latent block b into score buffer b, the rope (stored as
+      // rope / mant_0) into buffer 0 after block 0, once every gather warp has written the tile
+      ok = ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane, p.wait_ns) && ok;
+      ok = ptx::mbar_wait_warp(&ms.tile_full, 0, x.abort, lane, p.wait_ns) && ok;
+      if (ok) {
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          const uint64_t dK = desc_qk_operand(x.k_base), dQ = desc_qk_operand(x.q_base);
+          issue_qk<NH, 0, 2>(x.tmem + C::kSCol, dK, dQ);
+          issue_qk<NH, kRopeChunk, 1, true>(x.tmem + C::kSCol, dK, dQ);
+          ptx::mma_commit(&ms.s_full[0]);
+          issue_qk<NH, 2, 2>(x.tmem + C::kSCol + NH, dK, dQ);
+          ptx::mma_commit(&ms.s_full[1]);
+          issue_qk<NH, 4, 2>(x.tmem + C::kSCol + 2 * NH, dK, dQ);
+          ptx::mma_commit(&ms.s_full[2]);
+          issue_qk<NH, 6, 2>(x.tmem + C::kSCol + 3 * NH, dK, dQ);
+          ptx::mma_commit(&ms.s_full[3]);
+        }
+        __syncwarp();
+      }
+      // the QK MMAs are complete when this commit arrives (one of the two teardown arrivals)
+      if (ptx::elect_one()) ptx::mma_commit(&ms.teardown);
+      __syncwarp();
+    }
+  }
 }
 
 // ------------------------------------------------------------------------------------------ softmax
-template <int NH>
+template <int NH, bool kOneTile>
 __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
   using C = Cfg<NH>;
   constexpr int R = C::kR;
@@ -458,8 +491,8 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) mant[q] = ms.mant[q][t];
     // QK of latent block b into score buffer b, the rope (stored as rope / mant_0) into buffer 0
-    // after block 0; all 36 MMAs in one batch
-    if (issue_warp) {
+    // after block 0; all 36 MMAs in one batch (issued by gather warp 0 in one-tile launches)
+    if (issue_warp && !kOneTile) {
       if (i == 0) mma_ok = mma_ok && ptx::mbar_wait_warp(&ms.q_ready, 0, x.abort, lane, p.wait_ns);
       mma_ok = mma_ok && ok;
       if (mma_ok) {
@@ -854,8 +887,10 @@ __device__ __forceinline__ void fused_merge(const Ctx& x, int warp, int lane, bo
 }
 
 // kFused: the partitions of a (query, head group) form a cluster and merge inside the kernel; a separate
-// instantiation, so that the other launches carry none of that code.
-template <int NH, bool kFused>
+// instantiation, so that the other launches carry none of that code.  kOneTile: every partition holds at
+// most one tile (gather warp 0 issues its QK); also a separate instantiation, as the extra issue path
+// costs the multi-tile loop registers.
+template <int NH, bool kFused, bool kOneTile>
 __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p) {
   using C = Cfg<NH>;
   extern __shared__ unsigned char smem_raw[];
@@ -925,7 +960,7 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     for (int bb = 0; bb < 4; ++bb) ptx::mbar_init(&ms.s_full[bb], 1);
     ptx::mbar_init(&ms.pv0_done, 1);
     ptx::mbar_init(&ms.pv_done, 1);
-    ptx::mbar_init(&ms.teardown, 1);
+    ptx::mbar_init(&ms.teardown, kOneTile ? 2 : 1);   // one commit from each MMA-issuing thread
     ptx::mbar_init(&ms.merge_in, 1);
     ms.abort = 0;
     ms.range_err = 0;
@@ -952,8 +987,8 @@ __global__ void __launch_bounds__(kThreads, 1) split_kernel(const SplitParams p)
     ptx::bulk_g2s(x.k_base, p.q + ((size_t)x.b * p.H + (size_t)x.g * NH) * kDQK, qbytes, &ms.q_raw);
   }
 
-  if (warp >= kSoftWarps) gather_role(x, warp, lane);
-  else softmax_role<NH>(x, warp, lane);
+  if (warp >= kSoftWarps) gather_role<NH, kOneTile>(x, warp, lane);
+  else softmax_role<NH, kOneTile>(x, warp, lane);
 
   // ------------------------------------------------------------------ epilogue
   bool ok = ptx::mbar_wait_warp(&ms.pv_done, (x.n_tiles - 1) & 1, x.abort, lane, p.wait_ns);
@@ -1026,9 +1061,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
-// Kernel attributes of split_kernel<NH, kFused> on the current device: set once per device (a per-device flag,
-// read without a lock once set; the first call on a device configures it under the lock).
-template <int NH, bool kFused>
+// Kernel attributes of split_kernel<NH, kFused, kOneTile> on the current device: set once per device (a
+// per-device flag, read without a lock once set; the first call on a device configures it under the lock).
+template <int NH, bool kFused, bool kOneTile>
 cudaError_t configure_split_nh(int dev) {
   static std::atomic<bool> configured[kMaxDevices];
   static std::mutex mu;
@@ -1036,7 +1071,8 @@ cudaError_t configure_split_nh(int dev) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 0 && dev < kMaxDevices && configured[dev].load(std::memory_order_relaxed)) return cudaSuccess;
   cudaError_t e =
-      cudaFuncSetAttribute(split_kernel<NH, kFused>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes<NH>());
+      cudaFuncSetAttribute(split_kernel<NH, kFused, kOneTile>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)smem_bytes<NH>());
   if (e != cudaSuccess) return e;
   // the smallest shared-memory carveout that holds the CTA: the rest of the SM's SRAM is L1, where the
   // record loads in flight land (about 28 KB at 64 heads per CTA, 60 KB at 16 or 32)
@@ -1044,7 +1080,7 @@ cudaError_t configure_split_nh(int dev) {
   e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   if (e != cudaSuccess) return e;
   const int pct = (int)((100 * (smem_bytes<NH>() + 1024) + max_smem - 1) / max_smem);
-  e = cudaFuncSetAttribute(split_kernel<NH, kFused>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(split_kernel<NH, kFused, kOneTile>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            pct < 100 ? pct : 100);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDevices) configured[dev].store(true, std::memory_order_release);
@@ -1056,7 +1092,11 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  e = p.fused ? configure_split_nh<NH, true>(dev) : configure_split_nh<NH, false>(dev);
+  // every partition holds at most one tile (the in-kernel merge keeps the general instantiation: with
+  // both, the 64-head CTA spills registers)
+  const bool one = !p.fused && p.split_len <= kTile;
+  e = p.fused ? configure_split_nh<NH, true, false>(dev)
+              : (one ? configure_split_nh<NH, false, true>(dev) : configure_split_nh<NH, false, false>(dev));
   if (e != cudaSuccess) return e;
   const int head_groups = (p.H + NH - 1) / NH;
   dim3 grid(p.nsplit, head_groups, p.B);
@@ -1081,7 +1121,9 @@ cudaError_t launch_split_nh(const SplitParams& p, cudaStream_t stream) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return p.fused ? cudaLaunchKernelEx(&cfg, split_kernel<NH, true>, p) : cudaLaunchKernelEx(&cfg, split_kernel<NH, false>, p);
+  if (p.fused) return cudaLaunchKernelEx(&cfg, split_kernel<NH, true, false>, p);
+  return one ? cudaLaunchKernelEx(&cfg, split_kernel<NH, false, true>, p)
+             : cudaLaunchKernelEx(&cfg, split_kernel<NH, false, false>, p);
 }
 
 }  // namespace
