@@ -548,14 +548,29 @@ __device__ __forceinline__ void softmax_role(const Ctx& x, int warp, int lane) {
 #pragma unroll
     for (int h = 0; h < NH; ++h) s[h] = (ok && valid) ? s[h] : -CUDART_INF_F;
     bool need = false;
+    if (i > 0) {
 #pragma unroll
-    for (int k = 0; k < NH / 4; ++k) {
-      const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
-      need |= (s[4 * k] > m.x + kRescaleThreshold) | (s[4 * k + 1] > m.y + kRescaleThreshold) |
-              (s[4 * k + 2] > m.z + kRescaleThreshold) | (s[4 * k + 3] > m.w + kRescaleThreshold);
+      for (int k = 0; k < NH / 4; ++k) {
+        const float4 m = reinterpret_cast<const float4*>(ms.m_ref)[k];
+        need |= (s[4 * k] > m.x + kRescaleThreshold) | (s[4 * k + 1] > m.y + kRescaleThreshold) |
+                (s[4 * k + 2] > m.z + kRescaleThreshold) | (s[4 * k + 3] > m.w + kRescaleThreshold);
+      }
+      need = ptx::named_bar_or(3, kSoftThreads, need);
     }
-    need = ptx::named_bar_or(3, kSoftThreads, need);
-    if (need) {
+    if (i == 0) {
+      // first tile: a head's reference max is its tile max (no vote, nothing to rescale yet)
+      float mx[R];
+      reduce_scatter<true, NH>(s, lane, mx);
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+        if (NH >= 32 || (lane & 1) == 0) ms.red[warp][rs_head<NH>(lane, r)] = mx[r];
+      ptx::named_bar_sync(2, kSoftThreads);
+      if (warp == 0) {
+        for (int h = lane; h < NH; h += 32)
+          ms.m_ref[h] = fmaxf(fmaxf(ms.red[0][h], ms.red[1][h]), fmaxf(ms.red[2][h], ms.red[3][h]));
+      }
+      ptx::named_bar_sync(2, kSoftThreads);
+    } else if (need) {
       // a head's reference max moves to its tile max when that exceeds it by more than the threshold
       float mx[R];
       reduce_scatter<true, NH>(s, lane, mx);
