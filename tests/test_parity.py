@@ -58,6 +58,18 @@ def test_every_head_group_size(H, nsplit, nh):
     compare(out, lse, *oracle_on(w))
 
 
+@pytest.mark.parametrize("nh", [16, 32, 64])
+@pytest.mark.parametrize("topk", [256, 258])
+def test_one_tile_partitions_and_the_next_size(nh, topk):
+    # two partitions of 128 entries (every partition one tile: the launch takes the one-tile
+    # instantiation, whose QK gather warp 0 issues) and of 129 entries (the general instantiation)
+    w = _custom(B=3, H=64, topk=topk, ctx=[3000, 257, 129], seed=70 + nh + topk, outlier_channels=2)
+    out, lse = api.sparse_mla_decode(w.q, w.kv_cache, w.block_table, w.topk_idx, w.seq_lens, w.sm_scale,
+                                     nsplit=2, heads_per_cta=nh)
+    torch.cuda.synchronize()
+    compare(out, lse, *oracle_on(w))
+
+
 @pytest.mark.parametrize("H,nsplit", [(16, 4), (32, 8), (64, 5), (128, 3), (64, 2)])
 def test_split_merge_heads_and_partitions(H, nsplit):
     # head counts of one or two groups, partitions made only of padding (ctx 40 < topk), several
