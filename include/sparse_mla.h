@@ -79,7 +79,7 @@ typedef enum smla_status {
 #define SMLA_DEVERR_LEN_RANGE  0x8u  /* a top-k selection length outside [0, num_cols] was clamped */
 
 typedef struct smla_dims {
-  int32_t batch;              /* B >= 1 decode queries                                   */
+  int32_t batch;              /* B decode queries, 1 .. 65535                            */
   int32_t num_heads;          /* H in {16, 32, 64, 128}                                  */
   int32_t topk;               /* top-k entries per query, 1 .. 2048                      */
   int32_t page_size;          /* tokens per page; must be 64                             */

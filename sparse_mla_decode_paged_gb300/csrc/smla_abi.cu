@@ -31,7 +31,7 @@ int check_decode_dims(const smla_dims* d) {
     return SMLA_ERR_INVALID_ARG;
   if (d->merge < 0 || d->merge > 2) return SMLA_ERR_INVALID_ARG;
   if (d->page_size != kPageSize || d->d_latent != kDLatent || d->d_rope != kDRope) return SMLA_ERR_UNSUPPORTED;
-  if (d->topk > kMaxTopk || d->nsplit > kMaxSplit) return SMLA_ERR_UNSUPPORTED;
+  if (d->topk > kMaxTopk || d->nsplit > kMaxSplit || d->batch > kMaxBatch) return SMLA_ERR_UNSUPPORTED;
   if (!split_shape_supported(d->num_heads, d->topk)) return SMLA_ERR_UNSUPPORTED;
   return SMLA_OK;
 }

@@ -15,6 +15,7 @@ constexpr int kDQK = kDLatent + kDRope;   // 576
 constexpr int kRecordBytes = 656;
 constexpr int kMaxTopk = 2048;
 constexpr int kMaxSplit = 16;
+constexpr int kMaxBatch = 65535;      // decode queries per call (the split grid's z extent)
 constexpr int kMaxCombineSplit = 64;
 constexpr size_t kWorkspaceHeader = 256;
 constexpr int kMaxFusedSplit = 8;      // partitions merged inside the split kernel (one portable cluster)

@@ -57,6 +57,8 @@ def test_host_side_rejections(lib):
     assert _decode(lib, bad) == 2                                     # top-k too long
     bad = make_dims(0, 64, 512, 16, 100, nsplit=4)
     assert _decode(lib, bad) == 1
+    bad = make_dims(65536, 64, 512, 16, 100, nsplit=4)
+    assert _decode(lib, bad) == 2                                     # more queries than the grid holds
     need = lib.sparse_mla_workspace_size(C.byref(d), 4)
     assert need == 256 + 4 * 4 * 64 * 4 + 4 * 4 * 64 * 512 * 4
     assert _decode(lib, d, ws_bytes=need - 1) == 3                    # workspace too small
